@@ -1,0 +1,197 @@
+/*
+ * ep.h -- C ABI of the GB300 MoE expert-parallel dispatch / combine library.
+ *
+ * What it computes (the pages describe DeepEP's operations in prose only):
+ *  - "DeepEP 要約" (stakiran.github.io), section 3 "使うときの流れ":
+ *    training / prefill forward is get_dispatch_layout -> dispatch(x,
+ *    topk_idx, topk_weights, ...) -> expert computation -> combine(y, handle);
+ *    the backward of dispatch is combine and the backward of combine is
+ *    dispatch, both reusing the handle; decode uses low_latency_dispatch and
+ *    low_latency_combine, which are CUDA-graph compatible.
+ *  - "DeepSeek công bố thư viện mã nguồn mở DeepEP cho huấn luyện và suy luận
+ *    MoE" (vi.news.hada.io), section "Mẫu sử dụng cho huấn luyện, prefill và
+ *    decoding": dispatch routes tokens to the experts of every rank (BF16 or
+ *    FP8), the handle carries the routing metadata that combine needs and the
+ *    per-expert receive counts for the grouped GEMM; combine reduces the
+ *    expert outputs back to the originating rank; a cached handle avoids
+ *    recomputing the layout and the CPU synchronisation.
+ *  - "Как DeepSeek разогнали обмен данными в своих нейросетях" (devtrends.ru),
+ *    section "Как это выглядит в коде": the dispatch and low_latency_dispatch
+ *    call shapes; section "Что умеет DeepEP": the number of SMs the kernels
+ *    occupy is under the caller's control.
+ *  - "DeepSeek выпустила DeepEP V2.5" (aikraft.ru), section "Технические
+ *    детали и требования": FP8 dispatch, BF16 combine.
+ *
+ * One GPU.  The R expert-parallel ranks are logical partitions of one HBM:
+ * source rank s owns tokens [s*T/R, (s+1)*T/R); rank r owns experts
+ * [r*E_l, (r+1)*E_l) with E_l = E/R.  The all-to-all is a device-wide
+ * permutation; there is no communication library underneath.
+ *
+ * Conventions for every call
+ *  - Pointers marked "dev" are device pointers on the device that was
+ *    current when the handle was created; "host" pointers are ordinary host
+ *    memory.  The caller owns every pointer it passes; the library keeps none
+ *    of them after the call returns.
+ *  - Tensors are row-major and contiguous.  bf16 is IEEE bfloat16 (2 bytes),
+ *    e4m3 is OCP FP8 E4M3 ("FN", max 448, no infinities), weights and scales
+ *    are IEEE binary32.  hidden (H) is a positive multiple of 128; FP8 scales
+ *    are one fp32 per 128 consecutive channels of a token (G = H/128 per row,
+ *    scale = amax/448, dequantised value = e4m3 * scale).
+ *  - Every device buffer must be 16-byte aligned.
+ *  - All work is enqueued on the caller's stream and is asynchronous unless a
+ *    call says it synchronises.  Calls on one handle must not overlap in
+ *    time (one stream per handle, or caller-side ordering).
+ *  - Argument errors return a status before anything is enqueued.
+ *    Conditions found on the device (an expert id outside [-1, E), a receive
+ *    buffer that is too small, a bounded wait that gave up) are latched in the
+ *    handle: the offending rows are skipped -- never written out of bounds --
+ *    and the first such status is returned (and cleared) by
+ *    ep_get_device_status() and also reported by ep_get_num_recv().
+ *  - No call allocates device memory after ep_handle_create().
+ */
+#ifndef GB300_EP_H_
+#define GB300_EP_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same underlying type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* ep_stream_t;
+
+typedef struct ep_handle* ep_handle_t;
+
+typedef enum {
+  EP_OK = 0,
+  EP_ERR_INVALID_ARG = 1, /* a bad size, pointer, alignment or dtype         */
+  EP_ERR_CUDA = 2,        /* a CUDA runtime call failed                       */
+  EP_ERR_CAPACITY = 3,    /* a receive buffer had fewer rows than needed     */
+  EP_ERR_BAD_EXPERT = 4,  /* topk_idx held an id outside [-1, E)             */
+  EP_ERR_TIMEOUT = 5,     /* a bounded cross-block wait gave up              */
+  EP_ERR_STATE = 6        /* e.g. dispatch before any layout on this handle */
+} ep_status_t;
+
+typedef enum { EP_BF16 = 0, EP_FP8_E4M3 = 1 } ep_dtype_t;
+
+/* Create a handle for R ranks, E experts (E % R == 0), top-k = num_topk
+ * (1..32), hidden size H (multiple of 128) and at most max_tokens_per_rank
+ * tokens per source rank (so T <= R * max_tokens_per_rank).  Allocates, once,
+ * the device metadata arena: routing maps, counts, the cross-block scan
+ * state and the error latch.  Limits: R <= 1024, E <= 4096.
+ * Cite: Buffer(group, ...) / ElasticBuffer creation ("DeepEP 要約" section 3;
+ * vi.news.hada.io "Giao diện xoay quanh ElasticBuffer"). */
+ep_status_t ep_handle_create(int num_ranks, int num_experts, int num_topk, int hidden,
+                             int max_tokens_per_rank, ep_handle_t* out);
+
+/* Free the handle's device and host memory.  The caller must make sure no
+ * enqueued work that uses the handle is still pending.  NULL is a no-op. */
+ep_status_t ep_handle_destroy(ep_handle_t h);
+
+/* get_dispatch_layout ("DeepEP 要約" section 3, training forward;
+ * devtrends.ru "Как это выглядит в коде", num_tokens_per_rank).
+ * In:  topk_idx   dev int64 [T][k]; -1 marks a masked entry.
+ *      T          number of tokens, a multiple of R, <= R*max_tokens_per_rank.
+ * Out (each may be NULL):
+ *      num_tokens_per_rank    dev int32 [R src][R dst]: tokens source rank s
+ *                             sends to rank r (a token counts once per rank);
+ *      num_tokens_per_expert  dev int32 [R src][E]: (token, k) entries of
+ *                             source rank s routed to expert e;
+ *      is_token_in_rank       dev uint8 (bool) [T][R].
+ * Also stores in the handle, for ep_dispatch / ep_combine: each token's
+ * destination ranks and its row inside every destination rank's region
+ * (rows ordered by source rank, then token), the regions' offsets inside the
+ * packed receive buffer and the per-rank / per-expert receive counts. */
+ep_status_t ep_get_dispatch_layout(ep_handle_t h, const int64_t* topk_idx, int num_tokens,
+                                   int* num_tokens_per_rank, int* num_tokens_per_expert,
+                                   uint8_t* is_token_in_rank, ep_stream_t stream);
+
+/* Copy the receive counts of the last layout to host memory; synchronises
+ * `stream`.  Out (each may be NULL): num_recv_tokens_per_rank host int32 [R],
+ * num_recv_tokens_per_expert host int32 [E] (handle.num_recv_tokens_per_expert_list
+ * for the grouped GEMM; vi.news.hada.io "Mẫu sử dụng ..."), rank_offset host
+ * int32 [R+1] (row where rank r's region starts in the packed receive buffer;
+ * rank_offset[R] = total rows P).  Returns the latched device status, if any
+ * (without clearing it). */
+ep_status_t ep_get_num_recv(ep_handle_t h, int* num_recv_tokens_per_rank,
+                            int* num_recv_tokens_per_expert, int* rank_offset,
+                            ep_stream_t stream);
+
+/* dispatch, normal mode ("DeepEP 要約" section 3; devtrends.ru "Как это
+ * выглядит в коде").  Uses the handle's last layout (so it also serves the
+ * backward of combine and a cached handle).
+ * In:  x            dev bf16 [T][H].
+ *      topk_weights dev fp32 [T][k] or NULL.
+ *      dtype        EP_BF16: rows are copied; EP_FP8_E4M3: each row is
+ *                   quantised once (per 128 channels: a = max(amax, 1e-4),
+ *                   scale = a/448, q = e4m3_rn_satfinite(x * (448/a))).
+ * Out: recv_x       dev [cap][H], bf16 or e4m3 bytes; rank r's rows start at
+ *                   rank_offset[r]; only the first P rows are written.
+ *      recv_scales  dev fp32 [cap][H/128] (FP8 only, else ignored).
+ *      recv_capacity_rows  cap; rows beyond it are skipped and latch
+ *                   EP_ERR_CAPACITY.
+ *      recv_src_idx       dev int32 [cap] or NULL: source token of each row.
+ *      recv_topk_idx      dev int32 [cap][k] or NULL: the token's expert id
+ *                         made local to the receiving rank, -1 if the expert
+ *                         lives elsewhere or is masked.
+ *      recv_topk_weights  dev fp32 [cap][k] or NULL (needs topk_weights):
+ *                         the weight where recv_topk_idx >= 0, else 0.
+ *      num_sms      SMs to occupy (0 = all). */
+ep_status_t ep_dispatch(ep_handle_t h, const void* x, const float* topk_weights, ep_dtype_t dtype,
+                        void* recv_x, float* recv_scales, int64_t recv_capacity_rows,
+                        int* recv_src_idx, int* recv_topk_idx, float* recv_topk_weights,
+                        int num_sms, ep_stream_t stream);
+
+/* combine, normal mode ("DeepEP 要約" section 3; vi.news.hada.io: combine
+ * reduces the expert outputs back to the originating rank).
+ * In:  y      dev bf16 [y_rows][H], laid out like dispatch's recv_x.
+ * Out: out    dev bf16 [T][H]: for each token, the fp32 sum of its rows over
+ *             its destination ranks in ascending rank order (from +0.0),
+ *             rounded to bf16 (nearest-even); 0 for a token sent nowhere.
+ * A source row at or past y_rows is skipped (counted as absent) and latches
+ * EP_ERR_CAPACITY; nothing is read out of bounds. */
+ep_status_t ep_combine(ep_handle_t h, const void* y, int64_t y_rows, void* out, int num_sms,
+                       ep_stream_t stream);
+
+/* low_latency_dispatch (devtrends.ru "Как это выглядит в коде";
+ * "DeepEP 要約" section 3, decode).  Computes its own routing (no separate
+ * layout call, no host synchronisation, capturable in a CUDA graph) and
+ * stores it in the handle for ep_low_latency_combine.
+ * In:  x         dev bf16 [T][H];  topk_idx dev int64 [T][k];  T as above.
+ * Out: recv_x       dev [E][M][H] (bf16 or e4m3), M = R * max_tokens_per_rank;
+ *                   expert e = (rank e / E_l, local expert e % E_l); the
+ *                   entries routed to e fill rows 0..count-1 in (source rank,
+ *                   token, k-index) order.
+ *      recv_scales  dev fp32 [E][M][H/128] (FP8 only).
+ *      recv_src_info dev int32 [E][M] or NULL: source token of each row.
+ *      recv_count   dev int32 [E] or NULL: rows filled per expert.
+ * Rows past M (only possible with duplicated ids in one token) are skipped
+ * and latch EP_ERR_CAPACITY. */
+ep_status_t ep_low_latency_dispatch(ep_handle_t h, const void* x, const int64_t* topk_idx,
+                                    int num_tokens, ep_dtype_t dtype, void* recv_x,
+                                    float* recv_scales, int* recv_src_info, int* recv_count,
+                                    int num_sms, ep_stream_t stream);
+
+/* low_latency_combine ("DeepEP 要約" section 3, decode).  Uses the routing of
+ * the handle's last ep_low_latency_dispatch.
+ * In:  y            dev bf16 [E][M][H], laid out like that dispatch's recv_x.
+ *      topk_weights dev fp32 [T][k].
+ * Out: out          dev bf16 [T][H]: acc = fmaf(w, y, acc) over the token's
+ *                   unmasked entries in ascending expert id (k-index breaks
+ *                   ties), from +0.0, rounded to bf16 (nearest-even). */
+ep_status_t ep_low_latency_combine(ep_handle_t h, const void* y, const float* topk_weights,
+                                   void* out, int num_sms, ep_stream_t stream);
+
+/* Synchronise `stream`, then return and clear the first device-side status
+ * latched since the last call (EP_OK if none). */
+ep_status_t ep_get_device_status(ep_handle_t h, ep_stream_t stream);
+
+/* Static, NUL-terminated name of a status. */
+const char* ep_status_str(ep_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_EP_H_ */
