@@ -1,0 +1,443 @@
+// The C ABI declared in include/ep.h: handle lifecycle, argument checks,
+// launch configuration and the device status latch.  Every step of the
+// computation runs in this library's kernels; there is no host fallback.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "ep.h"
+#include "ep_internal.h"
+#include "routing.cuh"
+
+struct ep_handle {
+  int R, E, k, H, max_tpr, El, kmax, kp_log2;
+  int Tmax;
+  int device, num_sms;
+  // routing configuration
+  int layout_CT, ll_CT;
+  size_t layout_smem, ll_smem;
+  int layout_cmax, ll_cmax;
+  // occupancy (blocks per SM) of the persistent kernels
+  int occ_dispatch[2], occ_combine[2];
+  // state
+  int T_layout;  // tokens of the last layout, -1 before the first
+  int T_ll;      // tokens of the last low-latency dispatch, -1 before the first
+  bool debug;
+  // device arena
+  void* arena;
+  int2* dst;
+  int* idx32;
+  int* rank_offset;
+  int* recv_per_rank;
+  int* recv_per_expert;
+  int* ll_idx;
+  int* ll_slot;
+  unsigned long long* layout_flags;
+  unsigned long long* ll_flags;
+  unsigned long long* tickets;  // [0] layout, [1] low latency: (epoch << 32) | next chunk id
+  int* err;
+  // pinned host mirror: err, then R + E + R+1 counts
+  int* host;
+};
+
+namespace {
+
+using ep::RouteParams;
+
+ep_status_t cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return EP_OK;
+  if (std::getenv("EP_DEBUG")) std::fprintf(stderr, "[ep] %s: %s\n", what, cudaGetErrorString(e));
+  return EP_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned8(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+ep_status_t check_device(const ep_handle* h) {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess) return EP_ERR_CUDA;
+  return d == h->device ? EP_OK : EP_ERR_INVALID_ARG;
+}
+
+int grid_for(const ep_handle* h, int occ, int num_sms, int T, int warps_per_block) {
+  int sms = num_sms <= 0 ? h->num_sms : (num_sms < h->num_sms ? num_sms : h->num_sms);
+  int blocks = sms * (occ > 0 ? occ : 1);
+  int need = ceil_div(T, warps_per_block);
+  if (need < blocks) blocks = need;
+  return blocks > 0 ? blocks : 1;
+}
+
+RouteParams route_params(ep_handle* h, const int64_t* topk_idx, int T, int CT,
+                         unsigned long long* flags, unsigned long long* ticket) {
+  RouteParams p;
+  p.topk_idx = topk_idx;
+  p.T = T;
+  p.R = h->R;
+  p.E = h->E;
+  p.El = h->El;
+  p.k = h->k;
+  p.kp_log2 = h->kp_log2;
+  p.kmax = h->kmax;
+  p.tpr = T / h->R;
+  p.CT = CT;
+  p.cps = ceil_div(p.tpr, CT);
+  p.C = h->R * p.cps;
+  p.flags = flags;
+  p.ticket = ticket;
+  p.err = h->err;
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ep_status_str(ep_status_t s) {
+  switch (s) {
+    case EP_OK: return "EP_OK";
+    case EP_ERR_INVALID_ARG: return "EP_ERR_INVALID_ARG";
+    case EP_ERR_CUDA: return "EP_ERR_CUDA";
+    case EP_ERR_CAPACITY: return "EP_ERR_CAPACITY";
+    case EP_ERR_BAD_EXPERT: return "EP_ERR_BAD_EXPERT";
+    case EP_ERR_TIMEOUT: return "EP_ERR_TIMEOUT";
+    case EP_ERR_STATE: return "EP_ERR_STATE";
+  }
+  return "EP_ERR_UNKNOWN";
+}
+
+ep_status_t ep_handle_create(int R, int E, int k, int H, int max_tpr, ep_handle_t* out) {
+  if (!out) return EP_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (R < 1 || R > 1024 || E < 1 || E > 4096 || E % R != 0 || k < 1 || k > 32 || H < 128 ||
+      H % 128 != 0 || max_tpr < 1)
+    return EP_ERR_INVALID_ARG;
+  if (static_cast<long long>(R) * max_tpr > (1LL << 30)) return EP_ERR_INVALID_ARG;
+
+  ep_handle* h = new (std::nothrow) ep_handle();
+  if (!h) return EP_ERR_CUDA;
+  h->R = R;
+  h->E = E;
+  h->k = k;
+  h->H = H;
+  h->max_tpr = max_tpr;
+  h->El = E / R;
+  h->kmax = k < R ? k : R;
+  int kp = 1, lg = 0;
+  while (kp < k) kp <<= 1, ++lg;
+  h->kp_log2 = lg;
+  h->Tmax = R * max_tpr;
+  h->T_layout = -1;
+  h->T_ll = -1;
+  h->debug = std::getenv("EP_DEBUG") != nullptr;
+
+  ep_status_t st = EP_OK;
+  cudaDeviceProp prop;
+  if ((st = cuda_status(cudaGetDevice(&h->device), "cudaGetDevice")) != EP_OK ||
+      (st = cuda_status(cudaGetDeviceProperties(&prop, h->device), "cudaGetDeviceProperties")) != EP_OK) {
+    delete h;
+    return st;
+  }
+  h->num_sms = prop.multiProcessorCount;
+
+  // routing chunks: 1024 (token, k) items per layout block, 8 tokens per
+  // low-latency block (decode batches are small; more blocks, more SMs)
+  h->layout_CT = 1024 >> lg;
+  h->ll_CT = 8;
+  const int NKl = R + E, NKll = E;
+  h->layout_smem = ep::route_smem_bytes(NKl, h->layout_CT << lg, h->layout_CT, h->kmax);
+  h->ll_smem = ep::route_smem_bytes(NKll, h->ll_CT << lg, h->ll_CT, h->kmax);
+  if (h->layout_smem > static_cast<size_t>(prop.sharedMemPerBlockOptin) ||
+      h->ll_smem + 1024 > static_cast<size_t>(prop.sharedMemPerBlockOptin)) {
+    delete h;
+    return EP_ERR_INVALID_ARG;
+  }
+  h->layout_cmax = R * ceil_div(max_tpr, h->layout_CT);
+  h->ll_cmax = R * ceil_div(max_tpr, h->ll_CT);
+
+  // one device arena for all metadata
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = off;
+    off += (bytes + 255) & ~static_cast<size_t>(255);
+    return at;
+  };
+  const size_t o_dst = take(sizeof(int2) * static_cast<size_t>(h->Tmax) * h->kmax);
+  const size_t o_idx = take(sizeof(int) * static_cast<size_t>(h->Tmax) * k);
+  const size_t o_off = take(sizeof(int) * (R + 1));
+  const size_t o_rpr = take(sizeof(int) * R);
+  const size_t o_rpe = take(sizeof(int) * E);
+  const size_t o_llidx = take(sizeof(int) * static_cast<size_t>(h->Tmax) * k);
+  const size_t o_llslot = take(sizeof(int) * static_cast<size_t>(h->Tmax) * k);
+  const size_t o_lf = take(sizeof(unsigned long long) * static_cast<size_t>(h->layout_cmax) * NKl);
+  const size_t o_llf = take(sizeof(unsigned long long) * static_cast<size_t>(h->ll_cmax) * NKll);
+  const size_t o_tk = take(sizeof(unsigned long long) * 2);
+  const size_t o_err = take(sizeof(int));
+  if ((st = cuda_status(cudaMalloc(&h->arena, off), "cudaMalloc")) != EP_OK) {
+    delete h;
+    return st;
+  }
+  char* base = static_cast<char*>(h->arena);
+  h->dst = reinterpret_cast<int2*>(base + o_dst);
+  h->idx32 = reinterpret_cast<int*>(base + o_idx);
+  h->rank_offset = reinterpret_cast<int*>(base + o_off);
+  h->recv_per_rank = reinterpret_cast<int*>(base + o_rpr);
+  h->recv_per_expert = reinterpret_cast<int*>(base + o_rpe);
+  h->ll_idx = reinterpret_cast<int*>(base + o_llidx);
+  h->ll_slot = reinterpret_cast<int*>(base + o_llslot);
+  h->layout_flags = reinterpret_cast<unsigned long long*>(base + o_lf);
+  h->ll_flags = reinterpret_cast<unsigned long long*>(base + o_llf);
+  h->tickets = reinterpret_cast<unsigned long long*>(base + o_tk);
+  h->err = reinterpret_cast<int*>(base + o_err);
+  // zero everything once (latch, look-back words); tickets start at epoch 1,
+  // so no look-back word ever matches before it is written
+  const unsigned long long first_ticket[2] = {1ull << 32, 1ull << 32};
+  if ((st = cuda_status(cudaMemset(h->arena, 0, off), "cudaMemset")) != EP_OK ||
+      (st = cuda_status(cudaMemcpy(h->tickets, first_ticket, sizeof(first_ticket), cudaMemcpyHostToDevice),
+                        "cudaMemcpy")) != EP_OK ||
+      (st = cuda_status(cudaMallocHost(&h->host, sizeof(int) * (1 + 2 * R + E + 1)), "cudaMallocHost")) != EP_OK) {
+    cudaFree(h->arena);
+    delete h;
+    return st;
+  }
+  if ((st = cuda_status(ep::configure_layout(h->layout_smem), "configure_layout")) != EP_OK ||
+      (st = cuda_status(ep::configure_ll_dispatch(h->ll_smem), "configure_ll_dispatch")) != EP_OK) {
+    ep_handle_destroy(h);
+    return st;
+  }
+  for (int m = 0; m < 2; ++m) {
+    int occ = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, ep::dispatch_kernel(m == 1), ep::dispatch_threads(), 0);
+    h->occ_dispatch[m] = occ > 0 ? occ : 1;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, ep::combine_kernel(m == 1), ep::combine_threads(), 0);
+    h->occ_combine[m] = occ > 0 ? occ : 1;
+  }
+  if (h->debug)
+    std::fprintf(stderr,
+                 "[ep] handle R=%d E=%d k=%d H=%d max_tokens_per_rank=%d on device %d (%d SMs); "
+                 "layout chunk %d tokens (%zu B smem), ll chunk %d tokens (%zu B smem); "
+                 "blocks/SM dispatch bf16 %d fp8 %d, combine %d ll-combine %d; arena %zu B\n",
+                 R, E, k, H, max_tpr, h->device, h->num_sms, h->layout_CT, h->layout_smem, h->ll_CT,
+                 h->ll_smem, h->occ_dispatch[0], h->occ_dispatch[1], h->occ_combine[0], h->occ_combine[1], off);
+  *out = h;
+  return EP_OK;
+}
+
+ep_status_t ep_handle_destroy(ep_handle_t h) {
+  if (!h) return EP_OK;
+  if (h->arena) cudaFree(h->arena);
+  if (h->host) cudaFreeHost(h->host);
+  delete h;
+  return EP_OK;
+}
+
+ep_status_t ep_get_dispatch_layout(ep_handle_t h, const int64_t* topk_idx, int T, int* num_tokens_per_rank,
+                                   int* num_tokens_per_expert, uint8_t* is_token_in_rank, ep_stream_t stream) {
+  if (!h) return EP_ERR_INVALID_ARG;
+  if (T < 0 || T % h->R != 0 || T > h->Tmax || (T > 0 && !topk_idx)) return EP_ERR_INVALID_ARG;
+  if ((topk_idx && !aligned8(topk_idx)) || (num_tokens_per_rank && !aligned4(num_tokens_per_rank)) ||
+      (num_tokens_per_expert && !aligned4(num_tokens_per_expert)))
+    return EP_ERR_INVALID_ARG;
+  ep_status_t st = check_device(h);
+  if (st != EP_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    // nothing to route: every count is zero
+    cudaError_t e = cudaMemsetAsync(h->rank_offset, 0, sizeof(int) * (h->R + 1), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->recv_per_rank, 0, sizeof(int) * h->R, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->recv_per_expert, 0, sizeof(int) * h->E, s);
+    if (e == cudaSuccess && num_tokens_per_rank)
+      e = cudaMemsetAsync(num_tokens_per_rank, 0, sizeof(int) * h->R * h->R, s);
+    if (e == cudaSuccess && num_tokens_per_expert)
+      e = cudaMemsetAsync(num_tokens_per_expert, 0, sizeof(int) * static_cast<size_t>(h->R) * h->E, s);
+    if ((st = cuda_status(e, "layout memset")) != EP_OK) return st;
+    h->T_layout = 0;
+    return EP_OK;
+  }
+  RouteParams p = route_params(h, topk_idx, T, h->layout_CT, h->layout_flags, h->tickets + 0);
+  ep::LayoutOutPtrs o{h->dst, h->idx32, h->recv_per_rank, h->rank_offset, h->recv_per_expert,
+                      num_tokens_per_rank, num_tokens_per_expert, is_token_in_rank};
+  ep::launch_layout(p, o, h->layout_smem, s);
+  if ((st = cuda_status(cudaGetLastError(), "k_layout launch")) != EP_OK) return st;
+  if (h->debug) std::fprintf(stderr, "[ep] layout T=%d: %d blocks x %d threads\n", T, p.C, ep::kRouteThreads);
+  h->T_layout = T;
+  return EP_OK;
+}
+
+ep_status_t ep_get_num_recv(ep_handle_t h, int* num_recv_tokens_per_rank, int* num_recv_tokens_per_expert,
+                            int* rank_offset, ep_stream_t stream) {
+  if (!h) return EP_ERR_INVALID_ARG;
+  if (h->T_layout < 0) return EP_ERR_STATE;
+  ep_status_t st = check_device(h);
+  if (st != EP_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int* hp = h->host;
+  cudaError_t e = cudaMemcpyAsync(hp, h->err, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(hp + 1, h->recv_per_rank, sizeof(int) * h->R, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(hp + 1 + h->R, h->recv_per_expert, sizeof(int) * h->E, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(hp + 1 + h->R + h->E, h->rank_offset, sizeof(int) * (h->R + 1), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if ((st = cuda_status(e, "ep_get_num_recv")) != EP_OK) return st;
+  if (num_recv_tokens_per_rank) std::memcpy(num_recv_tokens_per_rank, hp + 1, sizeof(int) * h->R);
+  if (num_recv_tokens_per_expert) std::memcpy(num_recv_tokens_per_expert, hp + 1 + h->R, sizeof(int) * h->E);
+  if (rank_offset) std::memcpy(rank_offset, hp + 1 + h->R + h->E, sizeof(int) * (h->R + 1));
+  return static_cast<ep_status_t>(hp[0]);
+}
+
+ep_status_t ep_dispatch(ep_handle_t h, const void* x, const float* topk_weights, ep_dtype_t dtype, void* recv_x,
+                        float* recv_scales, int64_t cap, int* recv_src_idx, int* recv_topk_idx,
+                        float* recv_topk_weights, int num_sms, ep_stream_t stream) {
+  if (!h) return EP_ERR_INVALID_ARG;
+  if (h->T_layout < 0) return EP_ERR_STATE;
+  if (dtype != EP_BF16 && dtype != EP_FP8_E4M3) return EP_ERR_INVALID_ARG;
+  const bool fp8 = dtype == EP_FP8_E4M3;
+  const int T = h->T_layout;
+  if (cap < 0 || (cap > 0 && !recv_x) || (fp8 && cap > 0 && !recv_scales) || (T > 0 && !x))
+    return EP_ERR_INVALID_ARG;
+  if (recv_topk_weights && !topk_weights) return EP_ERR_INVALID_ARG;
+  if ((x && !aligned16(x)) || (recv_x && !aligned16(recv_x)) || (fp8 && recv_scales && !aligned4(recv_scales)) ||
+      (topk_weights && !aligned4(topk_weights)) || (recv_src_idx && !aligned4(recv_src_idx)) ||
+      (recv_topk_idx && !aligned4(recv_topk_idx)) || (recv_topk_weights && !aligned4(recv_topk_weights)))
+    return EP_ERR_INVALID_ARG;
+  ep_status_t st = check_device(h);
+  if (st != EP_OK) return st;
+  if (T == 0) return EP_OK;
+  ep::DispatchArgs a;
+  a.x = static_cast<const uint16_t*>(x);
+  a.topk_weights = topk_weights;
+  a.dst = h->dst;
+  a.idx32 = h->idx32;
+  a.rank_offset = h->rank_offset;
+  a.recv_x = recv_x;
+  a.recv_scales = recv_scales;
+  a.recv_src_idx = recv_src_idx;
+  a.recv_topk_idx = recv_topk_idx;
+  a.recv_topk_weights = recv_topk_weights;
+  a.cap = cap;
+  a.T = T;
+  a.H = h->H;
+  a.k = h->k;
+  a.kmax = h->kmax;
+  a.El = h->El;
+  a.err = h->err;
+  const int blocks = grid_for(h, h->occ_dispatch[fp8 ? 1 : 0], num_sms, T, ep::dispatch_threads() / 32);
+  ep::launch_dispatch(a, fp8, blocks, reinterpret_cast<cudaStream_t>(stream));
+  if (h->debug) std::fprintf(stderr, "[ep] dispatch %s T=%d: %d blocks\n", fp8 ? "fp8" : "bf16", T, blocks);
+  return cuda_status(cudaGetLastError(), "k_dispatch launch");
+}
+
+ep_status_t ep_combine(ep_handle_t h, const void* y, int64_t y_rows, void* out, int num_sms, ep_stream_t stream) {
+  if (!h) return EP_ERR_INVALID_ARG;
+  if (h->T_layout < 0) return EP_ERR_STATE;
+  const int T = h->T_layout;
+  if (y_rows < 0 || (T > 0 && (!out || (y_rows > 0 && !y)))) return EP_ERR_INVALID_ARG;
+  if ((y && !aligned16(y)) || (out && !aligned16(out))) return EP_ERR_INVALID_ARG;
+  ep_status_t st = check_device(h);
+  if (st != EP_OK) return st;
+  if (T == 0) return EP_OK;
+  ep::CombineArgs a{};
+  a.y = static_cast<const uint16_t*>(y);
+  a.out = static_cast<uint16_t*>(out);
+  a.y_rows = y_rows;
+  a.T = T;
+  a.H = h->H;
+  a.k = h->k;
+  a.kmax = h->kmax;
+  a.dst = h->dst;
+  a.rank_offset = h->rank_offset;
+  a.err = h->err;
+  const int blocks = grid_for(h, h->occ_combine[0], num_sms, T, ep::combine_threads() / 32);
+  ep::launch_combine(a, false, blocks, reinterpret_cast<cudaStream_t>(stream));
+  if (h->debug) std::fprintf(stderr, "[ep] combine T=%d: %d blocks\n", T, blocks);
+  return cuda_status(cudaGetLastError(), "k_combine launch");
+}
+
+ep_status_t ep_low_latency_dispatch(ep_handle_t h, const void* x, const int64_t* topk_idx, int T, ep_dtype_t dtype,
+                                    void* recv_x, float* recv_scales, int* recv_src_info, int* recv_count,
+                                    int num_sms, ep_stream_t stream) {
+  if (!h) return EP_ERR_INVALID_ARG;
+  if (dtype != EP_BF16 && dtype != EP_FP8_E4M3) return EP_ERR_INVALID_ARG;
+  const bool fp8 = dtype == EP_FP8_E4M3;
+  if (T < 0 || T % h->R != 0 || T > h->Tmax) return EP_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !topk_idx || !recv_x || (fp8 && !recv_scales))) return EP_ERR_INVALID_ARG;
+  if ((x && !aligned16(x)) || (topk_idx && !aligned8(topk_idx)) || (recv_x && !aligned16(recv_x)) ||
+      (fp8 && recv_scales && !aligned4(recv_scales)) || (recv_src_info && !aligned4(recv_src_info)) ||
+      (recv_count && !aligned4(recv_count)))
+    return EP_ERR_INVALID_ARG;
+  ep_status_t st = check_device(h);
+  if (st != EP_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int M = h->Tmax;
+  if (T == 0) {
+    h->T_ll = 0;
+    if (recv_count) return cuda_status(cudaMemsetAsync(recv_count, 0, sizeof(int) * h->E, s), "ll memset");
+    return EP_OK;
+  }
+  (void)num_sms;  // one block per chunk of ll_CT tokens; see the header
+  RouteParams p = route_params(h, topk_idx, T, h->ll_CT, h->ll_flags, h->tickets + 1);
+  ep::LowLatencyOut o;
+  o.x = static_cast<const uint16_t*>(x);
+  o.recv_x = recv_x;
+  o.recv_scales = recv_scales;
+  o.recv_src_info = recv_src_info;
+  o.recv_count = recv_count;
+  o.ll_idx = h->ll_idx;
+  o.ll_slot = h->ll_slot;
+  o.H = h->H;
+  o.M = M;
+  ep::launch_ll_dispatch(p, o, fp8, h->ll_smem, s);
+  if ((st = cuda_status(cudaGetLastError(), "k_ll_dispatch launch")) != EP_OK) return st;
+  if (h->debug) std::fprintf(stderr, "[ep] ll dispatch T=%d: %d blocks\n", T, p.C);
+  h->T_ll = T;
+  return EP_OK;
+}
+
+ep_status_t ep_low_latency_combine(ep_handle_t h, const void* y, const float* topk_weights, void* out, int num_sms,
+                                   ep_stream_t stream) {
+  if (!h) return EP_ERR_INVALID_ARG;
+  if (h->T_ll < 0) return EP_ERR_STATE;
+  const int T = h->T_ll;
+  if (T > 0 && (!y || !topk_weights || !out)) return EP_ERR_INVALID_ARG;
+  if ((y && !aligned16(y)) || (out && !aligned16(out)) || (topk_weights && !aligned4(topk_weights)))
+    return EP_ERR_INVALID_ARG;
+  ep_status_t st = check_device(h);
+  if (st != EP_OK) return st;
+  if (T == 0) return EP_OK;
+  ep::CombineArgs a{};
+  a.y = static_cast<const uint16_t*>(y);
+  a.out = static_cast<uint16_t*>(out);
+  a.y_rows = static_cast<long long>(h->E) * h->Tmax;
+  a.T = T;
+  a.H = h->H;
+  a.k = h->k;
+  a.kmax = h->kmax;
+  a.ll_idx = h->ll_idx;
+  a.ll_slot = h->ll_slot;
+  a.topk_weights = topk_weights;
+  a.M = h->Tmax;
+  a.err = h->err;
+  const int blocks = grid_for(h, h->occ_combine[1], num_sms, T, ep::combine_threads() / 32);
+  ep::launch_combine(a, true, blocks, reinterpret_cast<cudaStream_t>(stream));
+  if (h->debug) std::fprintf(stderr, "[ep] ll combine T=%d: %d blocks\n", T, blocks);
+  return cuda_status(cudaGetLastError(), "k_combine(ll) launch");
+}
+
+ep_status_t ep_get_device_status(ep_handle_t h, ep_stream_t stream) {
+  if (!h) return EP_ERR_INVALID_ARG;
+  ep_status_t st = check_device(h);
+  if (st != EP_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(h->host, h->err, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->err, 0, sizeof(int), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if ((st = cuda_status(e, "ep_get_device_status")) != EP_OK) return st;
+  return static_cast<ep_status_t>(h->host[0]);
+}
+
+}  // extern "C"

@@ -1,0 +1,81 @@
+// Host-side declarations shared by the library's translation units: the
+// kernel launchers each .cu file exports to the C-ABI layer (api.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ep {
+
+struct RouteParams;  // routing.cuh
+
+struct LayoutOutPtrs {
+  int2* dst;
+  int* idx32;
+  int* recv_per_rank;
+  int* rank_offset;
+  int* recv_per_expert;
+  int* num_tokens_per_rank;
+  int* num_tokens_per_expert;
+  uint8_t* is_token_in_rank;
+};
+
+void launch_layout(const RouteParams& p, const LayoutOutPtrs& out, size_t smem, cudaStream_t stream);
+cudaError_t configure_layout(size_t smem);
+
+// Normal dispatch: one warp per token, persistent grid.
+struct DispatchArgs {
+  const uint16_t* x;           // [T][H] bf16
+  const float* topk_weights;   // [T][k] or null
+  const int2* dst;             // [T][kmax]
+  const int* idx32;            // [T][k]
+  const int* rank_offset;      // [R+1]
+  void* recv_x;                // [cap][H] bf16 or e4m3
+  float* recv_scales;          // [cap][H/128]
+  int* recv_src_idx;           // [cap] or null
+  int* recv_topk_idx;          // [cap][k] or null
+  float* recv_topk_weights;    // [cap][k] or null
+  long long cap;
+  int T, H, k, kmax, El;
+  int* err;
+};
+void launch_dispatch(const DispatchArgs& a, bool fp8, int blocks, cudaStream_t stream);
+int dispatch_threads();
+const void* dispatch_kernel(bool fp8);
+
+// Normal and low-latency combine: one warp per token.
+struct CombineArgs {
+  const uint16_t* y;           // rows of bf16 [.][H]
+  uint16_t* out;               // [T][H]
+  long long y_rows;
+  int T, H, k, kmax;
+  // normal mode
+  const int2* dst;             // [T][kmax]
+  const int* rank_offset;      // [R+1]
+  // low-latency mode
+  const int* ll_idx;           // [T][k]
+  const int* ll_slot;          // [T][k]
+  const float* topk_weights;   // [T][k]
+  int M;
+  int* err;
+};
+void launch_combine(const CombineArgs& a, bool low_latency, int blocks, cudaStream_t stream);
+int combine_threads();
+const void* combine_kernel(bool low_latency);
+
+// Fused low-latency dispatch: routing phase + per-chunk scatter.
+struct LowLatencyOut {
+  const uint16_t* x;
+  void* recv_x;                // [E][M][H]
+  float* recv_scales;          // [E][M][H/128]
+  int* recv_src_info;          // [E][M] or null
+  int* recv_count;             // [E] or null
+  int* ll_idx;                 // [T][k]
+  int* ll_slot;                // [T][k]
+  int H, M;
+};
+void launch_ll_dispatch(const RouteParams& p, const LowLatencyOut& o, bool fp8, size_t smem,
+                        cudaStream_t stream);
+cudaError_t configure_ll_dispatch(size_t smem);
+
+}  // namespace ep

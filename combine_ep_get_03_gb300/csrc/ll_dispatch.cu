@@ -1,0 +1,93 @@
+// low_latency_dispatch on sm_103a, one launch: each block ranks the entries
+// of a small chunk of tokens per expert (single-pass cross-block scan), then
+// writes its tokens -- quantised once to FP8 or copied as BF16 -- into the
+// expert-major receive buffer [E][M][H] ("Как DeepSeek разогнали обмен
+// данными ..." (devtrends.ru), "Как это выглядит в коде":
+// low_latency_dispatch(hidden_states, topk_idx, num_max_tokens, num_experts);
+// "DeepEP 要約" (stakiran.github.io) section 3, decode: no host
+// synchronisation, CUDA-graph compatible).
+//
+// Rows of expert e are filled in (source rank, token, k-index) order, so the
+// result does not depend on block scheduling.
+#include "ep_internal.h"
+#include "routing.cuh"
+#include "scatter.cuh"
+
+namespace ep {
+
+template <bool kFP8>
+__global__ void __launch_bounds__(kRouteThreads) k_ll_dispatch(RouteParams p, LowLatencyOut o) {
+  extern __shared__ int smem_raw[];
+  __shared__ float sscale[kRouteWarps][kSeg * 4];
+  const int NK = p.E;
+  const int NI = p.CT << p.kp_log2;
+  const RouteSmem s = route_smem_carve(smem_raw, NK, NI, p.CT, p.kmax);
+  const RouteTicket tk = route_take_ticket(p, s);
+  const int c = tk.chunk;
+  const int src = c / p.cps;
+  const int ci = c - src * p.cps;
+  const int t0 = src * p.tpr + ci * p.CT;
+  const int ct = min(p.CT, p.tpr - ci * p.CT);
+
+  route_rank_chunk<false>(p, s, t0, ct, NK);
+  route_lookback(p, s, c, tk.epoch, NK);
+
+  const int kp = 1 << p.kp_log2;
+  const int ipw = route_items_per_warp(NI);
+  for (int i = threadIdx.x; i < NI; i += kRouteThreads) {
+    const int tl = i >> p.kp_log2;
+    const int j = i & (kp - 1);
+    if (tl >= ct || j >= p.k) continue;
+    const int t = t0 + tl;
+    const int e = s.item_e[i];
+    int slot = -1;
+    if (e >= 0) {
+      slot = s.excl[e] + s.cnt[(i / ipw) * NK + e] + s.item_le[i];
+      if (slot >= o.M) {
+        latch_error(p.err, kErrCapacity);
+        slot = -1;
+      }
+    }
+    o.ll_idx[static_cast<size_t>(t) * p.k + j] = e;
+    o.ll_slot[static_cast<size_t>(t) * p.k + j] = slot;
+    s.item_le[i] = slot;
+  }
+  if (c == p.C - 1 && o.recv_count) {
+    for (int e = threadIdx.x; e < p.E; e += kRouteThreads) o.recv_count[e] = min(s.excl[e] + s.agg[e], o.M);
+  }
+  __syncthreads();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int tl = warp; tl < ct; tl += kRouteWarps) {
+    const int t = t0 + tl;
+    long long row = -1;
+    if (lane < p.k) {
+      const int i = (tl << p.kp_log2) + lane;
+      const int e = s.item_e[i];
+      const int sl = s.item_le[i];
+      if (e >= 0 && sl >= 0) row = static_cast<long long>(e) * o.M + sl;
+    }
+    const unsigned dmask = __ballot_sync(kFullMask, row >= 0);
+    scatter_row<kFP8>(o.x + static_cast<size_t>(t) * o.H, o.H, dmask, row, o.recv_x, o.recv_scales,
+                      sscale[warp], lane);
+    if (o.recv_src_info && row >= 0) o.recv_src_info[row] = t;
+  }
+}
+
+void launch_ll_dispatch(const RouteParams& p, const LowLatencyOut& o, bool fp8, size_t smem,
+                        cudaStream_t stream) {
+  if (fp8)
+    k_ll_dispatch<true><<<p.C, kRouteThreads, smem, stream>>>(p, o);
+  else
+    k_ll_dispatch<false><<<p.C, kRouteThreads, smem, stream>>>(p, o);
+}
+
+cudaError_t configure_ll_dispatch(size_t smem) {
+  cudaError_t e = cudaFuncSetAttribute(k_ll_dispatch<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_ll_dispatch<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(smem));
+}
+
+}  // namespace ep

@@ -1,0 +1,293 @@
+"""ctypes binding of ``libep_gb300.so`` -- the C ABI in ``include/ep.h``.
+
+Argument marshalling only: every function takes torch tensors (or None for a
+NULL pointer), checks dtype / device / contiguity, and passes raw device
+pointers and the current CUDA stream to the library call of the same name.
+All computation happens in the library's CUDA kernels; if the library is
+missing this module raises instead of computing anything itself.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libep_gb300.so")
+
+EP_OK, EP_ERR_INVALID_ARG, EP_ERR_CUDA, EP_ERR_CAPACITY, EP_ERR_BAD_EXPERT, EP_ERR_TIMEOUT, EP_ERR_STATE = range(7)
+EP_BF16, EP_FP8_E4M3 = 0, 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class EPError(RuntimeError):
+    def __init__(self, status: int, call: str):
+        super().__init__(f"{call}: {status_str(status)} ({status})")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Load the CUDA library (raises if it was not built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build the CUDA library first "
+                    "(python -m combine_ep_get_03_gb300.build); there is no fallback path")
+            L = ctypes.CDLL(LIB_PATH)
+            P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+            L.ep_handle_create.argtypes = [I, I, I, I, I, ctypes.POINTER(P)]
+            L.ep_handle_destroy.argtypes = [P]
+            L.ep_get_dispatch_layout.argtypes = [P, P, I, P, P, P, P]
+            L.ep_get_num_recv.argtypes = [P, P, P, P, P]
+            L.ep_dispatch.argtypes = [P, P, P, I, P, P, I64, P, P, P, I, P]
+            L.ep_combine.argtypes = [P, P, I64, P, I, P]
+            L.ep_low_latency_dispatch.argtypes = [P, P, P, I, I, P, P, P, P, I, P]
+            L.ep_low_latency_combine.argtypes = [P, P, P, P, I, P]
+            L.ep_get_device_status.argtypes = [P, P]
+            L.ep_status_str.argtypes = [I]
+            L.ep_status_str.restype = ctypes.c_char_p
+            for n in ("ep_handle_create", "ep_handle_destroy", "ep_get_dispatch_layout", "ep_get_num_recv",
+                      "ep_dispatch", "ep_combine", "ep_low_latency_dispatch", "ep_low_latency_combine",
+                      "ep_get_device_status"):
+                getattr(L, n).restype = I
+            _lib = L
+    return _lib
+
+
+def status_str(s: int) -> str:
+    return lib().ep_status_str(int(s)).decode()
+
+
+ep_status_str = status_str
+
+
+def _check(status: int, call: str) -> int:
+    if status != EP_OK:
+        raise EPError(status, call)
+    return status
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t, dtypes=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor or None")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    return t.data_ptr()
+
+
+_FP8_BYTES = (torch.uint8, torch.float8_e4m3fn)
+
+
+# ------------------------------------------------------------------ calls
+
+def ep_handle_create(num_ranks: int, num_experts: int, num_topk: int, hidden: int,
+                     max_tokens_per_rank: int) -> int:
+    h = ctypes.c_void_p()
+    _check(lib().ep_handle_create(num_ranks, num_experts, num_topk, hidden, max_tokens_per_rank,
+                                  ctypes.byref(h)), "ep_handle_create")
+    return h.value
+
+
+def ep_handle_destroy(h: int) -> None:
+    _check(lib().ep_handle_destroy(h), "ep_handle_destroy")
+
+
+def ep_get_dispatch_layout(h, topk_idx, num_tokens_per_rank=None, num_tokens_per_expert=None,
+                           is_token_in_rank=None, stream=None) -> None:
+    T = topk_idx.shape[0]
+    _check(lib().ep_get_dispatch_layout(
+        h, _ptr(topk_idx, (torch.int64,), "topk_idx"), T,
+        _ptr(num_tokens_per_rank, (torch.int32,), "num_tokens_per_rank"),
+        _ptr(num_tokens_per_expert, (torch.int32,), "num_tokens_per_expert"),
+        _ptr(is_token_in_rank, (torch.bool, torch.uint8), "is_token_in_rank"),
+        _stream(stream)), "ep_get_dispatch_layout")
+
+
+def ep_get_num_recv(h, num_ranks: int, num_experts: int, stream=None, check: bool = True):
+    """-> (num_recv_tokens_per_rank [R], num_recv_tokens_per_expert [E],
+    rank_offset [R+1]) as numpy int32, plus the latched device status."""
+    a = np.zeros(num_ranks, np.int32)
+    b = np.zeros(num_experts, np.int32)
+    c = np.zeros(num_ranks + 1, np.int32)
+    st = lib().ep_get_num_recv(h, a.ctypes.data, b.ctypes.data, c.ctypes.data, _stream(stream))
+    if check:
+        _check(st, "ep_get_num_recv")
+    return a, b, c, st
+
+
+def ep_dispatch(h, x, topk_weights, dtype: int, recv_x, recv_scales=None, recv_src_idx=None,
+                recv_topk_idx=None, recv_topk_weights=None, num_sms: int = 0, stream=None) -> None:
+    fp8 = dtype == EP_FP8_E4M3
+    cap = recv_x.shape[0] if recv_x is not None else 0
+    _check(lib().ep_dispatch(
+        h, _ptr(x, (torch.bfloat16,), "x"), _ptr(topk_weights, (torch.float32,), "topk_weights"), int(dtype),
+        _ptr(recv_x, _FP8_BYTES if fp8 else (torch.bfloat16,), "recv_x"),
+        _ptr(recv_scales, (torch.float32,), "recv_scales") if fp8 else None, cap,
+        _ptr(recv_src_idx, (torch.int32,), "recv_src_idx"),
+        _ptr(recv_topk_idx, (torch.int32,), "recv_topk_idx"),
+        _ptr(recv_topk_weights, (torch.float32,), "recv_topk_weights"),
+        int(num_sms), _stream(stream)), "ep_dispatch")
+
+
+def ep_combine(h, y, out, num_sms: int = 0, stream=None) -> None:
+    _check(lib().ep_combine(h, _ptr(y, (torch.bfloat16,), "y"), y.shape[0],
+                            _ptr(out, (torch.bfloat16,), "out"), int(num_sms), _stream(stream)), "ep_combine")
+
+
+def ep_low_latency_dispatch(h, x, topk_idx, dtype: int, recv_x, recv_scales=None, recv_src_info=None,
+                            recv_count=None, num_sms: int = 0, stream=None) -> None:
+    fp8 = dtype == EP_FP8_E4M3
+    _check(lib().ep_low_latency_dispatch(
+        h, _ptr(x, (torch.bfloat16,), "x"), _ptr(topk_idx, (torch.int64,), "topk_idx"), topk_idx.shape[0],
+        int(dtype), _ptr(recv_x, _FP8_BYTES if fp8 else (torch.bfloat16,), "recv_x"),
+        _ptr(recv_scales, (torch.float32,), "recv_scales") if fp8 else None,
+        _ptr(recv_src_info, (torch.int32,), "recv_src_info"), _ptr(recv_count, (torch.int32,), "recv_count"),
+        int(num_sms), _stream(stream)), "ep_low_latency_dispatch")
+
+
+def ep_low_latency_combine(h, y, topk_weights, out, num_sms: int = 0, stream=None) -> None:
+    _check(lib().ep_low_latency_combine(
+        h, _ptr(y, (torch.bfloat16,), "y"), _ptr(topk_weights, (torch.float32,), "topk_weights"),
+        _ptr(out, (torch.bfloat16,), "out"), int(num_sms), _stream(stream)), "ep_low_latency_combine")
+
+
+def ep_get_device_status(h, stream=None) -> int:
+    """Synchronise, then return and clear the latched device status."""
+    return lib().ep_get_device_status(h, _stream(stream))
+
+
+class Handle:
+    """Owns one ep_handle_t; methods call the ABI functions of the same name
+    after checking that every buffer is large enough for the call."""
+
+    def __init__(self, num_ranks, num_experts, num_topk, hidden, max_tokens_per_rank):
+        self.R, self.E, self.k, self.H = num_ranks, num_experts, num_topk, hidden
+        self.max_tokens_per_rank = max_tokens_per_rank
+        self.T = None      # tokens of the last layout
+        self.T_ll = None   # tokens of the last low-latency dispatch
+        self.ptr = ep_handle_create(num_ranks, num_experts, num_topk, hidden, max_tokens_per_rank)
+
+    @property
+    def M(self) -> int:
+        """Rows per expert in the low-latency receive buffer."""
+        return self.R * self.max_tokens_per_rank
+
+    @property
+    def G(self) -> int:
+        return self.H // 128
+
+    def close(self):
+        if getattr(self, "ptr", None):
+            ep_handle_destroy(self.ptr)
+            self.ptr = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    @staticmethod
+    def _need(t, n, name):
+        if t is not None and t.numel() < n:
+            raise ValueError(f"{name} holds {t.numel()} elements, the call needs {n}")
+
+    def get_dispatch_layout(self, topk_idx, num_tokens_per_rank=None, num_tokens_per_expert=None,
+                            is_token_in_rank=None, stream=None):
+        T = topk_idx.shape[0]
+        if topk_idx.dim() != 2 or topk_idx.shape[1] != self.k:
+            raise ValueError(f"topk_idx must be [T, {self.k}]")
+        self._need(num_tokens_per_rank, self.R * self.R, "num_tokens_per_rank")
+        self._need(num_tokens_per_expert, self.R * self.E, "num_tokens_per_expert")
+        self._need(is_token_in_rank, T * self.R, "is_token_in_rank")
+        ep_get_dispatch_layout(self.ptr, topk_idx, num_tokens_per_rank, num_tokens_per_expert,
+                               is_token_in_rank, stream)
+        self.T = T
+
+    def get_num_recv(self, stream=None, check=True):
+        return ep_get_num_recv(self.ptr, self.R, self.E, stream=stream, check=check)
+
+    def dispatch(self, x, topk_weights, dtype, recv_x, recv_scales=None, recv_src_idx=None,
+                 recv_topk_idx=None, recv_topk_weights=None, num_sms=0, stream=None):
+        if self.T is None:
+            raise RuntimeError("dispatch before any layout on this handle")
+        cap = recv_x.shape[0]
+        if recv_x.dim() != 2 or recv_x.shape[1] != self.H:
+            raise ValueError(f"recv_x must be [cap, {self.H}]")
+        self._need(x, self.T * self.H, "x")
+        self._need(topk_weights, self.T * self.k, "topk_weights")
+        if dtype == EP_FP8_E4M3:
+            if recv_scales is None:
+                raise ValueError("FP8 dispatch needs recv_scales")
+            self._need(recv_scales, cap * self.G, "recv_scales")
+        self._need(recv_src_idx, cap, "recv_src_idx")
+        self._need(recv_topk_idx, cap * self.k, "recv_topk_idx")
+        self._need(recv_topk_weights, cap * self.k, "recv_topk_weights")
+        ep_dispatch(self.ptr, x, topk_weights, dtype, recv_x, recv_scales, recv_src_idx, recv_topk_idx,
+                    recv_topk_weights, num_sms, stream)
+
+    def combine(self, y, out, num_sms=0, stream=None):
+        if self.T is None:
+            raise RuntimeError("combine before any layout on this handle")
+        if y.dim() != 2 or y.shape[1] != self.H:
+            raise ValueError(f"y must be [rows, {self.H}]")
+        self._need(out, self.T * self.H, "out")
+        ep_combine(self.ptr, y, out, num_sms, stream)
+
+    def low_latency_dispatch(self, x, topk_idx, dtype, recv_x, recv_scales=None, recv_src_info=None,
+                             recv_count=None, num_sms=0, stream=None):
+        T = topk_idx.shape[0]
+        if topk_idx.dim() != 2 or topk_idx.shape[1] != self.k:
+            raise ValueError(f"topk_idx must be [T, {self.k}]")
+        rows = self.E * self.M
+        self._need(x, T * self.H, "x")
+        if recv_x.numel() < rows * self.H:
+            raise ValueError(f"recv_x must hold [E, M, H] = [{self.E}, {self.M}, {self.H}]")
+        if dtype == EP_FP8_E4M3:
+            if recv_scales is None:
+                raise ValueError("FP8 dispatch needs recv_scales")
+            self._need(recv_scales, rows * self.G, "recv_scales")
+        self._need(recv_src_info, rows, "recv_src_info")
+        self._need(recv_count, self.E, "recv_count")
+        ep_low_latency_dispatch(self.ptr, x, topk_idx, dtype, recv_x, recv_scales, recv_src_info, recv_count,
+                                num_sms, stream)
+        self.T_ll = T
+
+    def low_latency_combine(self, y, topk_weights, out, num_sms=0, stream=None):
+        if self.T_ll is None:
+            raise RuntimeError("low-latency combine before any low-latency dispatch")
+        if y.numel() < self.E * self.M * self.H:
+            raise ValueError(f"y must hold [E, M, H] = [{self.E}, {self.M}, {self.H}]")
+        self._need(topk_weights, self.T_ll * self.k, "topk_weights")
+        self._need(out, self.T_ll * self.H, "out")
+        ep_low_latency_combine(self.ptr, y, topk_weights, out, num_sms, stream)
+
+    def get_device_status(self, stream=None):
+        return ep_get_device_status(self.ptr, stream)

@@ -79,7 +79,8 @@ typedef enum { EP_BF16 = 0, EP_FP8_E4M3 = 1 } ep_dtype_t;
  * (1..32), hidden size H (multiple of 128) and at most max_tokens_per_rank
  * tokens per source rank (so T <= R * max_tokens_per_rank).  Allocates, once,
  * the device metadata arena: routing maps, counts, the cross-block scan
- * state and the error latch.  Limits: R <= 1024, E <= 4096.
+ * state and the error latch.  Limits: R <= 1024, E <= 4096, and the
+ * per-block routing tables must fit in shared memory (EP_ERR_INVALID_ARG).
  * Cite: Buffer(group, ...) / ElasticBuffer creation ("DeepEP 要約" section 3;
  * vi.news.hada.io "Giao diện xoay quanh ElasticBuffer"). */
 ep_status_t ep_handle_create(int num_ranks, int num_experts, int num_topk, int hidden,
@@ -167,7 +168,9 @@ ep_status_t ep_combine(ep_handle_t h, const void* y, int64_t y_rows, void* out, 
  *      recv_src_info dev int32 [E][M] or NULL: source token of each row.
  *      recv_count   dev int32 [E] or NULL: rows filled per expert.
  * Rows past M (only possible with duplicated ids in one token) are skipped
- * and latch EP_ERR_CAPACITY. */
+ * and latch EP_ERR_CAPACITY.
+ * num_sms is accepted for symmetry and not used: the kernel runs one block
+ * per 8-token chunk, which at decode sizes is fewer blocks than SMs. */
 ep_status_t ep_low_latency_dispatch(ep_handle_t h, const void* x, const int64_t* topk_idx,
                                     int num_tokens, ep_dtype_t dtype, void* recv_x,
                                     float* recv_scales, int* recv_src_info, int* recv_count,
