@@ -130,7 +130,7 @@ def layout(R, E, k, topk_idx):
     out = dict(
         num_tokens_per_rank=np.zeros((R, R), np.int32),
         num_tokens_per_expert=np.zeros((R, E), np.int32),
-        is_token_in_rank=np.zeros((T, R), np.uint8),
+        is_token_in_rank=np.zeros((T, R), np.uint8),   # 0/1 bytes, as written
         slot=np.zeros((T, R), np.int32),
         num_recv_per_rank=np.zeros(R, np.int32),
         rank_offset=np.zeros(R + 1, np.int32),
@@ -139,7 +139,6 @@ def layout(R, E, k, topk_idx):
     _check(_load().ref_layout(R, E, k, T, _p(idx), *(_p(out[n]) for n in (
         "num_tokens_per_rank", "num_tokens_per_expert", "is_token_in_rank", "slot",
         "num_recv_per_rank", "rank_offset", "num_recv_per_expert"))))
-    out["is_token_in_rank"] = out["is_token_in_rank"].astype(bool)
     return out
 
 

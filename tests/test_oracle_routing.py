@@ -108,6 +108,30 @@ def test_low_latency_hand_worked(golden_dir):
     assert np.array_equal(_f32(comb), np.repeat(np.array(h["ll_combine_out_value"], np.float32)[:, None], H, 1))
 
 
+def test_combine_order_hand_worked(golden_dir):
+    """Summation order is observable: only ascending rank order keeps 2^-30."""
+    c = _hand(golden_dir)["combine_order"]
+    H = 128
+    idx = np.array(c["topk_idx"], np.int64)
+    y = _bf16(np.repeat(np.array(c["y_row_value"], np.float32)[:, None], H, 1))
+    out = oracle.combine(c["R"], c["E"], c["k"], idx, y)
+    assert np.array_equal(_f32(out), np.repeat(np.array(c["out_value"], np.float32)[:, None], H, 1))
+    assert not np.signbit(_f32(out[1:])).any()
+
+
+def test_ll_combine_order_hand_worked(golden_dir):
+    """Low-latency combine order is observable: only ascending expert id keeps 2^-30."""
+    c = _hand(golden_dir)["ll_combine_order"]
+    H, E, M = 128, c["E"], c["M"]
+    idx = np.array(c["topk_idx"], np.int64)
+    w = np.array(c["topk_weights"], np.float32)
+    y = np.zeros((E, M, H), np.uint16)
+    for e, v in enumerate(c["y_row0_value"]):
+        y[e, 0] = _bf16(np.full(H, v, np.float32))
+    out = oracle.ll_combine(c["R"], E, c["k"], M, idx, w, y)
+    assert np.array_equal(_f32(out), np.repeat(np.array(c["out_value"], np.float32)[:, None], H, 1))
+
+
 # ----------------------------------------------------------- brute force
 
 @pytest.mark.parametrize("T,R,E,k,mask,dup", [(64, 4, 16, 2, 0.0, 0.0), (96, 8, 64, 6, 0.05, 0.1),
@@ -127,7 +151,7 @@ def test_layout_vs_sorted_pairs(T, R, E, k, mask, dup):
     for pos, (t, r) in enumerate(pairs):
         slot[t, r] = pos - L["rank_offset"][r]
     assert np.array_equal(L["slot"], slot)
-    assert np.array_equal(L["is_token_in_rank"], slot >= 0)
+    assert np.array_equal(L["is_token_in_rank"], (slot >= 0).astype(np.uint8))
     # per-expert counts: bincount of the unmasked ids, by source rank
     tpr = T // R if R else 0
     for s in range(R):
