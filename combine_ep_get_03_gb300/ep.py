@@ -51,11 +51,12 @@ def lib() -> ctypes.CDLL:
             L.ep_low_latency_dispatch.argtypes = [P, P, P, I, I, P, P, P, P, I, P]
             L.ep_low_latency_combine.argtypes = [P, P, P, P, I, P]
             L.ep_get_device_status.argtypes = [P, P]
+            L.ep_get_dispatch_layout_noalloc.argtypes = [I, I, I, P, I, P, P, P, P, P, P, P, P, P, P]
             L.ep_status_str.argtypes = [I]
             L.ep_status_str.restype = ctypes.c_char_p
             for n in ("ep_handle_create", "ep_handle_destroy", "ep_get_dispatch_layout", "ep_get_num_recv",
                       "ep_dispatch", "ep_combine", "ep_low_latency_dispatch", "ep_low_latency_combine",
-                      "ep_get_device_status"):
+                      "ep_get_device_status", "ep_get_dispatch_layout_noalloc"):
                 getattr(L, n).restype = I
             _lib = L
     return _lib
@@ -175,6 +176,35 @@ def ep_low_latency_combine(h, y, topk_weights, out, num_sms: int = 0, stream=Non
 def ep_get_device_status(h, stream=None) -> int:
     """Synchronise, then return and clear the latched device status."""
     return lib().ep_get_device_status(h, _stream(stream))
+
+
+def ep_get_dispatch_layout_noalloc(num_ranks, num_experts, num_topk, topk_idx, num_recv_tokens_per_rank,
+                                   num_recv_tokens_per_expert, rank_offset, token_dest, topk_idx32,
+                                   num_tokens_per_rank=None, num_tokens_per_expert=None, is_token_in_rank=None,
+                                   device_status=None, stream=None) -> None:
+    """The handle-free, allocation-free layout: every output is a caller tensor
+    (see include/ep.h for shapes); the scan state lives in the library."""
+    T = topk_idx.shape[0]
+    R, E, k = num_ranks, num_experts, num_topk
+    kmax = min(k, R)
+    for t, n, name in ((num_recv_tokens_per_rank, R, "num_recv_tokens_per_rank"),
+                       (num_recv_tokens_per_expert, E, "num_recv_tokens_per_expert"),
+                       (rank_offset, R + 1, "rank_offset"), (token_dest, T * kmax * 2, "token_dest"),
+                       (topk_idx32, T * k, "topk_idx32"), (num_tokens_per_rank, R * R, "num_tokens_per_rank"),
+                       (num_tokens_per_expert, R * E, "num_tokens_per_expert"),
+                       (is_token_in_rank, T * R, "is_token_in_rank"), (device_status, 1, "device_status")):
+        if t is not None and t.numel() < n:
+            raise ValueError(f"{name} holds {t.numel()} elements, the call needs {n}")
+    _check(lib().ep_get_dispatch_layout_noalloc(
+        R, E, k, _ptr(topk_idx, (torch.int64,), "topk_idx"), T,
+        _ptr(num_tokens_per_rank, (torch.int32,), "num_tokens_per_rank"),
+        _ptr(num_tokens_per_expert, (torch.int32,), "num_tokens_per_expert"),
+        _ptr(is_token_in_rank, (torch.bool, torch.uint8), "is_token_in_rank"),
+        _ptr(num_recv_tokens_per_rank, (torch.int32,), "num_recv_tokens_per_rank"),
+        _ptr(num_recv_tokens_per_expert, (torch.int32,), "num_recv_tokens_per_expert"),
+        _ptr(rank_offset, (torch.int32,), "rank_offset"), _ptr(token_dest, (torch.int32,), "token_dest"),
+        _ptr(topk_idx32, (torch.int32,), "topk_idx32"), _ptr(device_status, (torch.int32,), "device_status"),
+        _stream(stream)), "ep_get_dispatch_layout_noalloc")
 
 
 class Handle:

@@ -186,6 +186,49 @@ ep_status_t ep_low_latency_dispatch(ep_handle_t h, const void* x, const int64_t*
 ep_status_t ep_low_latency_combine(ep_handle_t h, const void* y, const float* topk_weights,
                                    void* out, int num_sms, ep_stream_t stream);
 
+/* ep_get_dispatch_layout_noalloc -- the same layout computation as
+ * ep_get_dispatch_layout, for callers that cannot allocate device memory.
+ * The pages have no counterpart to this call; it exists for this library's
+ * users.  Some callers cannot call cudaMalloc at all: code that runs while a
+ * CUDA stream capture is in progress, serving runtimes that hand all device
+ * memory to their own allocator up front and forbid further allocations, and
+ * plugin hosts that call in per request with no place to keep a handle (whose
+ * creation allocates).  This entry point needs no handle and allocates
+ * nothing: every result goes to caller buffers, and the cross-block scan state
+ * lives in a fixed 1 MiB array in the library's device memory, which every GPU
+ * that loads the library holds until the process exits.
+ * Limits: R <= 1024, E <= 4096, E % R == 0, 1 <= k <= 32, T % R == 0, and
+ * R * ceil((T/R) / (1024 / k')) * (R + E) <= 131040, where k' is k rounded up
+ * to a power of two (V3 shape: 64 * 264; 64 ranks x 512 tokens: 256 * 320);
+ * larger sizes return EP_ERR_INVALID_ARG before anything is enqueued.
+ * The first call on a device looks up the array's device address (a one-time
+ * set-up per device); make that first call before any stream capture.
+ * Every call clears the part of the array it uses on `stream`, so calls on
+ * one device must not overlap on the GPU: two calls in flight at the same time
+ * (on different streams) race on the shared array.
+ * In:  topk_idx   dev int64 [T][k] (-1 = masked).
+ * Out (may be NULL): num_tokens_per_rank dev int32 [R][R],
+ *      num_tokens_per_expert dev int32 [R][E], is_token_in_rank dev uint8 [T][R]
+ *      -- as ep_get_dispatch_layout.
+ * Out (required): num_recv_tokens_per_rank dev int32 [R],
+ *      num_recv_tokens_per_expert dev int32 [E], rank_offset dev int32 [R+1],
+ *      token_dest dev int32 [T][min(k,R)][2] (8-byte aligned): each token's
+ *      destination ranks in ascending order as (rank, row inside the rank's
+ *      region), padded with (-1, -1); topk_idx32 dev int32 [T][k]: the ids as
+ *      int32 (bad ids as -1).  The global receive row of (t, r) is
+ *      rank_offset[r] + row.
+ *      device_status dev int32 [1] or NULL: if given (zeroed by the caller),
+ *      receives the first device-side status (EP_ERR_BAD_EXPERT,
+ *      EP_ERR_TIMEOUT); if NULL such statuses are dropped.  Bad ids are
+ *      treated as masked either way. */
+ep_status_t ep_get_dispatch_layout_noalloc(int num_ranks, int num_experts, int num_topk,
+                                           const int64_t* topk_idx, int num_tokens,
+                                           int* num_tokens_per_rank, int* num_tokens_per_expert,
+                                           uint8_t* is_token_in_rank, int* num_recv_tokens_per_rank,
+                                           int* num_recv_tokens_per_expert, int* rank_offset,
+                                           int* token_dest, int* topk_idx32, int* device_status,
+                                           ep_stream_t stream);
+
 /* Synchronise `stream`, then return and clear the first device-side status
  * latched since the last call (EP_OK if none). */
 ep_status_t ep_get_device_status(ep_handle_t h, ep_stream_t stream);
