@@ -39,19 +39,20 @@ from combine_ep_get_03_gb300 import workloads as wl  # noqa: E402
 METRIC = "dispatch & combine logical GB/s and % of GB300 HBM roofline (V3 shape, 1 GPU)"
 UNIT = "GB/s"
 OPS = ["layout", "dispatch_fp8", "combine", "dispatch_bf16_bwd", "combine_bwd", "ll_dispatch_fp8", "ll_combine"]
-KERNEL_OF = {"layout": "k_layout", "dispatch_fp8": "k_dispatch<true>", "combine": "k_combine<false>",
-             "dispatch_bf16_bwd": "k_dispatch<false>", "combine_bwd": "k_combine<false>",
-             "ll_dispatch_fp8": "k_ll_dispatch<true>", "ll_combine": "k_combine<true>"}
-KERNEL_SOURCES = {"k_combine<false>": ["combine.cu", "device_common.cuh"],
-                  "k_combine<true>": ["combine.cu", "device_common.cuh"],
-                  "k_dispatch<true>": ["dispatch.cu", "scatter.cuh", "device_common.cuh"],
-                  "k_dispatch<false>": ["dispatch.cu", "scatter.cuh", "device_common.cuh"],
-                  "k_ll_dispatch<true>": ["ll_dispatch.cu", "routing.cuh", "scatter.cuh", "device_common.cuh"],
+KERNEL_OF = {"layout": "k_layout", "dispatch_fp8": "k_scatter<fp8>", "combine": "k_combine<normal>",
+             "dispatch_bf16_bwd": "k_scatter<bf16>", "combine_bwd": "k_combine<normal>",
+             "ll_dispatch_fp8": "k_ll_route+k_scatter<fp8,ll>", "ll_combine": "k_combine<ll>"}
+KERNEL_SOURCES = {"k_combine<normal>": ["combine.cu", "device_common.cuh"],
+                  "k_combine<ll>": ["combine.cu", "device_common.cuh"],
+                  "k_scatter<fp8>": ["scatter_tma.cu", "device_common.cuh"],
+                  "k_scatter<bf16>": ["scatter_tma.cu", "device_common.cuh"],
+                  "k_ll_route+k_scatter<fp8,ll>": ["ll_dispatch.cu", "routing.cuh", "scatter_tma.cu",
+                                                   "device_common.cuh"],
                   "k_layout": ["layout.cu", "routing.cuh", "device_common.cuh"]}
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
 # ncu capture of the V3-shaped workload, keyed by the kernel's source digest:
 # a kernel whose sources changed since its capture reports traffic = null.
-MEASURED_TRAFFIC = {}
+MEASURED_TRAFFIC = {"k_combine<normal>": ("620290b911f494ee", 712725248)}
 
 
 def kernel_digest(kernel: str) -> str:
@@ -295,6 +296,72 @@ def e2e_steps(step: Step, K: int, stream: torch.cuda.Stream):
     return dt, h2d, d2h
 
 
+def ll_decode_latency(dev: torch.device, reps: int = 200):
+    """Low-latency dispatch + combine on the decode workload (128 tokens per
+    rank x 8 ranks, hidden 7168, top-8, FP8), timed per call with CUDA events
+    (L2-warm: a decode step's working set is small) and as CUDA-graph replays."""
+    w = wl.WORKLOADS["ll_decode_ep8"]
+    x, idx, wts = wl.make_inputs(w)
+    x_d = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+    idx_d = torch.from_numpy(idx).to(dev)
+    w_d = torch.from_numpy(wts).to(dev)
+    h = ep.Handle(w.R, w.E, w.k, w.H, w.tokens_per_rank)
+    M, G = h.M, w.H // 128
+    recv = torch.empty((w.E, M, w.H), dtype=torch.uint8, device=dev)
+    scales = torch.empty((w.E, M, G), dtype=torch.float32, device=dev)
+    cnt = torch.empty(w.E, dtype=torch.int32, device=dev)
+    y = torch.randn((w.E, M, w.H), device=dev).to(torch.bfloat16)
+    out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+
+    def disp():
+        h.low_latency_dispatch(x_d, idx_d, ep.EP_FP8_E4M3, recv, scales, recv_count=cnt)
+
+    def comb():
+        h.low_latency_combine(y, w_d, out)
+
+    for _ in range(10):
+        disp()
+        comb()
+    torch.cuda.synchronize(dev)
+    res = {}
+    for name, fn in (("dispatch", disp), ("combine", comb)):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+        ev[0].record()
+        for i in range(reps):
+            fn()
+            ev[i + 1].record()
+        torch.cuda.synchronize(dev)
+        ts = sorted(ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(reps))
+        res[name + "_us"] = round(ts[len(ts) // 2], 2)
+    # the pair as graph replays (launch overhead amortised)
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(10):
+                disp()
+                comb()
+    torch.cuda.current_stream(dev).wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(20):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    pair_us = e0.elapsed_time(e1) * 1e3 / 200
+    n_ll = int(cnt.sum().item())
+    res["pair_graph_us"] = round(pair_us, 2)
+    res["logical_gbs_graph"] = round(n_ll * (w.H + 4 * G + 2 * w.H) / (pair_us / 1e6) / 1e9, 1)
+    res["workload"] = w.name
+    if h.get_device_status() != ep.EP_OK:
+        raise RuntimeError("device status after the decode timing")
+    h.close()
+    return res
+
+
 # ----------------------------------------------------------------- CPU (oracle) arm
 
 def oracle_step(w: wl.Workload, tpr_s: int, rep: int = 0):
@@ -392,7 +459,7 @@ def reduce_time_units(t: float, units: float, device, world: int):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="v3_ep8", choices=sorted(wl.WORKLOADS))
@@ -493,13 +560,18 @@ def main():
         "gpu_launches": len(OPS) * args.steps,
         "clocks": clocks,
     }
+    line["ll_decode"] = ll_decode_latency(dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tpr_s = max(1, w.tokens_per_rank // 8)
-        dt, lb = oracle_step(w, tpr_s)
-        line["cpu_baseline"] = {"value": round(lb / dt / 1e9, 4), "unit": UNIT, "cores": cpu_cores_used(),
-                                "kind": "oracle",
-                                "sample": f"one step over the first {tpr_s} of {w.tokens_per_rank} tokens per "
-                                          f"source rank ({w.R * tpr_s} tokens), {dt:.1f} s"}
+        # whole-batch oracle steps until about 10 s of CPU work (at most 3)
+        tpr_s = w.tokens_per_rank
+        dts, lb = [], 0
+        while len(dts) < 3 and sum(dts) < 10.0:
+            dt, lb = oracle_step(w, tpr_s, rep=len(dts))
+            dts.append(dt)
+        line["cpu_baseline"] = {"value": round(lb * len(dts) / sum(dts) / 1e9, 4), "unit": UNIT,
+                                "cores": cpu_cores_used(), "kind": "oracle",
+                                "sample": f"{len(dts)} whole step(s) over the {w.T}-token batch, "
+                                          f"{sum(dts):.1f} s of CPU time"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -16,10 +16,14 @@ struct ep_handle {
   int device, num_sms;
   // routing configuration
   int layout_CT, ll_CT;
-  size_t layout_smem, ll_smem;
+  size_t layout_smem, ll_smem, layout_tokens_smem;
   int layout_cmax, ll_cmax;
   // occupancy (blocks per SM) of the persistent kernels
   int occ_dispatch[2], occ_combine[2];
+  // TMA scatter: warps per block for [fp8][low_latency]; 0 = rows too long,
+  // the register-resident kernels are used instead
+  int scatter_warps[2][2];
+  size_t ll_route_smem;
   // state
   int T_layout;  // tokens of the last layout, -1 before the first
   int T_ll;      // tokens of the last low-latency dispatch, -1 before the first
@@ -143,11 +147,15 @@ ep_status_t ep_handle_create(int R, int E, int k, int H, int max_tpr, ep_handle_
   }
   h->num_sms = prop.multiProcessorCount;
 
-  // routing chunks: 1024 (token, k) items per layout block, 8 tokens per
-  // low-latency block (decode batches are small; more blocks, more SMs)
-  h->layout_CT = 1024 >> lg;
-  h->ll_CT = 8;
+  // routing chunks: 2048 (token, k) items per layout block (1024 when the
+  // per-block tables would not fit), 8 tokens per fused low-latency block
   const int NKl = R + E, NKll = E;
+  int items = ep::kRouteMaxItems;
+  while (items > 1024 &&
+         ep::route_smem_bytes(NKl, items, items >> lg, h->kmax) > static_cast<size_t>(prop.sharedMemPerBlockOptin))
+    items >>= 1;
+  h->layout_CT = items >> lg;
+  h->ll_CT = 8;
   h->layout_smem = ep::route_smem_bytes(NKl, h->layout_CT << lg, h->layout_CT, h->kmax);
   h->ll_smem = ep::route_smem_bytes(NKll, h->ll_CT << lg, h->ll_CT, h->kmax);
   if (h->layout_smem > static_cast<size_t>(prop.sharedMemPerBlockOptin) ||
@@ -155,7 +163,8 @@ ep_status_t ep_handle_create(int R, int E, int k, int H, int max_tpr, ep_handle_
     delete h;
     return EP_ERR_INVALID_ARG;
   }
-  h->layout_cmax = R * ceil_div(max_tpr, h->layout_CT);
+  h->layout_cmax = R * ceil_div(max_tpr, h->layout_CT < ep::kLayoutTokenChunk ? h->layout_CT : ep::kLayoutTokenChunk);
+  h->layout_tokens_smem = ep::layout_tokens_smem(R, E, ep::kLayoutTokenChunk, h->kmax);
   h->ll_cmax = R * ceil_div(max_tpr, h->ll_CT);
 
   // one device arena for all metadata
@@ -203,8 +212,18 @@ ep_status_t ep_handle_create(int R, int E, int k, int H, int max_tpr, ep_handle_
     delete h;
     return st;
   }
+  // low-latency routing runs on layout-sized chunks (its look-back words fit
+  // in the space sized for the fused kernel's smaller chunks)
+  h->ll_route_smem = ep::route_smem_bytes(NKll, h->layout_CT << lg, h->layout_CT, h->kmax);
+  const size_t optin = static_cast<size_t>(prop.sharedMemPerBlockOptin);
+  for (int f = 0; f < 2; ++f)
+    for (int l = 0; l < 2; ++l) h->scatter_warps[f][l] = ep::scatter_warps_for(H, R, f == 1, l == 1, optin);
   if ((st = cuda_status(ep::configure_layout(h->layout_smem), "configure_layout")) != EP_OK ||
-      (st = cuda_status(ep::configure_ll_dispatch(h->ll_smem), "configure_ll_dispatch")) != EP_OK) {
+      (st = cuda_status(ep::configure_ll_dispatch(h->ll_smem), "configure_ll_dispatch")) != EP_OK ||
+      (st = cuda_status(ep::configure_ll_route(h->ll_route_smem), "configure_ll_route")) != EP_OK ||
+      (R <= 64 &&
+       (st = cuda_status(ep::configure_layout_tokens(h->layout_tokens_smem), "configure_layout_tokens")) != EP_OK) ||
+      (st = cuda_status(ep::configure_scatter(optin), "configure_scatter")) != EP_OK) {
     ep_handle_destroy(h);
     return st;
   }
@@ -219,9 +238,11 @@ ep_status_t ep_handle_create(int R, int E, int k, int H, int max_tpr, ep_handle_
     std::fprintf(stderr,
                  "[ep] handle R=%d E=%d k=%d H=%d max_tokens_per_rank=%d on device %d (%d SMs); "
                  "layout chunk %d tokens (%zu B smem), ll chunk %d tokens (%zu B smem); "
-                 "blocks/SM dispatch bf16 %d fp8 %d, combine %d ll-combine %d; arena %zu B\n",
+                 "blocks/SM dispatch bf16 %d fp8 %d, combine %d ll-combine %d; scatter warps bf16 %d fp8 %d; "
+                 "arena %zu B\n",
                  R, E, k, H, max_tpr, h->device, h->num_sms, h->layout_CT, h->layout_smem, h->ll_CT,
-                 h->ll_smem, h->occ_dispatch[0], h->occ_dispatch[1], h->occ_combine[0], h->occ_combine[1], off);
+                 h->ll_smem, h->occ_dispatch[0], h->occ_dispatch[1], h->occ_combine[0], h->occ_combine[1],
+                 h->scatter_warps[0][0], h->scatter_warps[1][0], off);
   *out = h;
   return EP_OK;
 }
@@ -257,10 +278,16 @@ ep_status_t ep_get_dispatch_layout(ep_handle_t h, const int64_t* topk_idx, int T
     h->T_layout = 0;
     return EP_OK;
   }
-  RouteParams p = route_params(h, topk_idx, T, h->layout_CT, h->layout_flags, h->tickets + 0);
   ep::LayoutOutPtrs o{h->dst, h->idx32, h->recv_per_rank, h->rank_offset, h->recv_per_expert,
                       num_tokens_per_rank, num_tokens_per_expert, is_token_in_rank};
-  ep::launch_layout(p, o, h->layout_smem, s);
+  // R <= 64: one lane per token (rank masks); otherwise one lane per (token, k) entry
+  const bool by_token = h->R <= 64;
+  RouteParams p = route_params(h, topk_idx, T, by_token ? ep::kLayoutTokenChunk : h->layout_CT, h->layout_flags,
+                               h->tickets + 0);
+  if (by_token)
+    ep::launch_layout_tokens(p, o, s);
+  else
+    ep::launch_layout(p, o, h->layout_smem, s);
   if ((st = cuda_status(cudaGetLastError(), "k_layout launch")) != EP_OK) return st;
   if (h->debug) std::fprintf(stderr, "[ep] layout T=%d: %d blocks x %d threads\n", T, p.C, ep::kRouteThreads);
   h->T_layout = T;
@@ -308,6 +335,34 @@ ep_status_t ep_dispatch(ep_handle_t h, const void* x, const float* topk_weights,
   ep_status_t st = check_device(h);
   if (st != EP_OK) return st;
   if (T == 0) return EP_OK;
+  const int sw = h->scatter_warps[fp8 ? 1 : 0][0];
+  if (sw > 0) {
+    ep::ScatterArgs a{};
+    a.x = static_cast<const uint16_t*>(x);
+    a.T = T;
+    a.H = h->H;
+    a.k = h->k;
+    a.kmax = h->kmax;
+    a.El = h->El;
+    a.R = h->R;
+    a.dst = h->dst;
+    a.rank_offset = h->rank_offset;
+    a.cap = cap;
+    a.idx32 = h->idx32;
+    a.topk_weights = topk_weights;
+    a.recv_src_idx = recv_src_idx;
+    a.recv_topk_idx = recv_topk_idx;
+    a.recv_topk_weights = recv_topk_weights;
+    a.recv_x = recv_x;
+    a.recv_scales = recv_scales;
+    a.err = h->err;
+    const int blocks = grid_for(h, 1, num_sms, T, sw);
+    ep::launch_scatter(a, fp8, false, blocks, sw, reinterpret_cast<cudaStream_t>(stream));
+    if (h->debug)
+      std::fprintf(stderr, "[ep] dispatch %s T=%d: TMA scatter %d blocks x %d warps\n", fp8 ? "fp8" : "bf16", T,
+                   blocks, sw);
+    return cuda_status(cudaGetLastError(), "k_scatter launch");
+  }
   ep::DispatchArgs a;
   a.x = static_cast<const uint16_t*>(x);
   a.topk_weights = topk_weights;
@@ -349,10 +404,11 @@ ep_status_t ep_combine(ep_handle_t h, const void* y, int64_t y_rows, void* out, 
   a.H = h->H;
   a.k = h->k;
   a.kmax = h->kmax;
+  a.R = h->R;
   a.dst = h->dst;
   a.rank_offset = h->rank_offset;
   a.err = h->err;
-  const int blocks = grid_for(h, h->occ_combine[0], num_sms, T, ep::combine_threads() / 32);
+  const int blocks = grid_for(h, h->occ_combine[0], num_sms, T * ((h->H + 1023) / 1024), ep::combine_threads() / 32);
   ep::launch_combine(a, false, blocks, reinterpret_cast<cudaStream_t>(stream));
   if (h->debug) std::fprintf(stderr, "[ep] combine T=%d: %d blocks\n", T, blocks);
   return cuda_status(cudaGetLastError(), "k_combine launch");
@@ -379,7 +435,37 @@ ep_status_t ep_low_latency_dispatch(ep_handle_t h, const void* x, const int64_t*
     if (recv_count) return cuda_status(cudaMemsetAsync(recv_count, 0, sizeof(int) * h->E, s), "ll memset");
     return EP_OK;
   }
-  (void)num_sms;  // one block per chunk of ll_CT tokens; see the header
+  const int sw = h->scatter_warps[fp8 ? 1 : 0][1];
+  if (sw > 0) {
+    // routing (slots, counts) on layout-sized chunks, then the TMA scatter
+    RouteParams p = route_params(h, topk_idx, T, h->layout_CT, h->ll_flags, h->tickets + 1);
+    ep::LowLatencyOutPtrs ro{recv_count, h->ll_idx, h->ll_slot, M};
+    ep::launch_ll_route(p, ro, h->ll_route_smem, s);
+    if ((st = cuda_status(cudaGetLastError(), "k_ll_route launch")) != EP_OK) return st;
+    ep::ScatterArgs a{};
+    a.x = static_cast<const uint16_t*>(x);
+    a.T = T;
+    a.H = h->H;
+    a.k = h->k;
+    a.kmax = h->kmax;
+    a.El = h->El;
+    a.R = h->R;
+    a.ll_idx = h->ll_idx;
+    a.ll_slot = h->ll_slot;
+    a.M = M;
+    a.recv_src_info = recv_src_info;
+    a.recv_x = recv_x;
+    a.recv_scales = recv_scales;
+    a.err = h->err;
+    const int blocks = grid_for(h, 1, num_sms, T, sw);
+    ep::launch_scatter(a, fp8, true, blocks, sw, s);
+    if ((st = cuda_status(cudaGetLastError(), "k_scatter(ll) launch")) != EP_OK) return st;
+    if (h->debug)
+      std::fprintf(stderr, "[ep] ll dispatch T=%d: route %d blocks, TMA scatter %d blocks x %d warps\n", T, p.C,
+                   blocks, sw);
+    h->T_ll = T;
+    return EP_OK;
+  }
   RouteParams p = route_params(h, topk_idx, T, h->ll_CT, h->ll_flags, h->tickets + 1);
   ep::LowLatencyOut o;
   o.x = static_cast<const uint16_t*>(x);
@@ -421,8 +507,9 @@ ep_status_t ep_low_latency_combine(ep_handle_t h, const void* y, const float* to
   a.ll_slot = h->ll_slot;
   a.topk_weights = topk_weights;
   a.M = h->Tmax;
+  a.R = h->R;
   a.err = h->err;
-  const int blocks = grid_for(h, h->occ_combine[1], num_sms, T, ep::combine_threads() / 32);
+  const int blocks = grid_for(h, h->occ_combine[1], num_sms, T * ((h->H + 1023) / 1024), ep::combine_threads() / 32);
   ep::launch_combine(a, true, blocks, reinterpret_cast<cudaStream_t>(stream));
   if (h->debug) std::fprintf(stderr, "[ep] ll combine T=%d: %d blocks\n", T, blocks);
   return cuda_status(cudaGetLastError(), "k_combine(ll) launch");

@@ -9,9 +9,11 @@
 //                over t's unmasked entries in ascending expert id (k-index
 //                breaks ties), from +0.0.
 //
-// HBM-bound gather-reduce: one warp per token, a 512-channel slab at a
-// time; every source row of the slab is requested before any is summed, so
-// up to kMaxSrc x 1 KB is in flight per warp.
+// HBM-bound gather-reduce.  Work is split into (token, 1024-channel part)
+// items dealt round-robin to the warps of a persistent grid, so the last
+// round leaves few warps idle.  A warp takes a part 512 channels at a time
+// and requests every source row of the slab before summing any, so up to
+// kMaxSrc x 1 KB is in flight per warp.
 #include <climits>
 
 #include "device_common.cuh"
@@ -23,21 +25,32 @@ constexpr int kCombineThreads = 256;
 constexpr int kCombineWarps = kCombineThreads / 32;
 constexpr int kChunks = 2;   // 16-byte chunks per lane per slab: slab = 32 * 2 * 8 = 512 channels
 constexpr int kMaxSrc = 8;   // source rows loaded together
+constexpr int kPartChannels = 1024;  // channels of one work item
+constexpr int kMaxCachedRanks = 1024;
 
 template <bool kLL>
 __global__ void __launch_bounds__(kCombineThreads) k_combine(CombineArgs a) {
+  __shared__ int so[kMaxCachedRanks + 1];  // rank_offset (normal mode)
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int nw = gridDim.x * kCombineWarps;
   const unsigned lt = lanemask_lt();
-  for (int t = blockIdx.x * kCombineWarps + warp; t < a.T; t += nw) {
+  if (!kLL) {
+    for (int r = threadIdx.x; r <= a.R; r += kCombineThreads) so[r] = a.rank_offset[r];
+    __syncthreads();
+  }
+  const int parts = (a.H + kPartChannels - 1) / kPartChannels;
+  const long long items = static_cast<long long>(a.T) * parts;
+  for (long long item = blockIdx.x * kCombineWarps + warp; item < items; item += nw) {
+    const int t = static_cast<int>(item / parts);
+    const int part = static_cast<int>(item - static_cast<long long>(t) * parts);
     long long row = -1;
     float w = 0.0f;
     int key = INT_MAX;
     if (!kLL) {
       if (lane < a.kmax) {
         const int2 d = a.dst[static_cast<size_t>(t) * a.kmax + lane];
-        if (d.x >= 0) row = static_cast<long long>(a.rank_offset[d.x]) + d.y;
+        if (d.x >= 0) row = static_cast<long long>(so[d.x]) + d.y;
       }
     } else if (lane < a.k) {
       const int e = a.ll_idx[static_cast<size_t>(t) * a.k + lane];
@@ -78,7 +91,8 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine(CombineArgs a) {
 
     const uint16_t* y = a.y;
     uint16_t* out = a.out + static_cast<size_t>(t) * a.H;
-    for (int h0 = 0; h0 < a.H; h0 += 32 * kChunks * 8) {
+    const int h_end = min(a.H, (part + 1) * kPartChannels);
+    for (int h0 = part * kPartChannels; h0 < h_end; h0 += 32 * kChunks * 8) {
       float acc[kChunks][8];
 #pragma unroll
       for (int c = 0; c < kChunks; ++c)
@@ -93,7 +107,7 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine(CombineArgs a) {
 #pragma unroll
             for (int c = 0; c < kChunks; ++c) {
               const int ch = h0 + (c * 32 + lane) * 8;
-              v[s][c] = ch < a.H ? ld_stream(y + r_ * a.H + ch) : make_uint4(0, 0, 0, 0);
+              v[s][c] = ch < h_end ? ld_stream(y + r_ * a.H + ch) : make_uint4(0, 0, 0, 0);
             }
           }
         }
@@ -121,7 +135,7 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine(CombineArgs a) {
 #pragma unroll
       for (int c = 0; c < kChunks; ++c) {
         const int ch = h0 + (c * 32 + lane) * 8;
-        if (ch < a.H) {
+        if (ch < h_end) {
           const uint4 o = make_uint4(pack_bf16x2(acc[c][0], acc[c][1]), pack_bf16x2(acc[c][2], acc[c][3]),
                                      pack_bf16x2(acc[c][4], acc[c][5]), pack_bf16x2(acc[c][6], acc[c][7]));
           st_na(out + ch, o);

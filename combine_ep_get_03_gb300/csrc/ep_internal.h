@@ -9,6 +9,13 @@ namespace ep {
 
 struct RouteParams;  // routing.cuh
 
+struct LowLatencyOutPtrs {
+  int* recv_count;  // [E] or null
+  int* ll_idx;      // [T][k]
+  int* ll_slot;     // [T][k]
+  int M;
+};
+
 struct LayoutOutPtrs {
   int2* dst;
   int* idx32;
@@ -22,6 +29,11 @@ struct LayoutOutPtrs {
 
 void launch_layout(const RouteParams& p, const LayoutOutPtrs& out, size_t smem, cudaStream_t stream);
 cudaError_t configure_layout(size_t smem);
+// token-per-lane layout (R <= 64)
+constexpr int kLayoutTokenChunk = 256;
+void launch_layout_tokens(const RouteParams& p, const LayoutOutPtrs& out, cudaStream_t stream);
+size_t layout_tokens_smem(int R, int E, int CT, int kmax);
+cudaError_t configure_layout_tokens(size_t smem);
 
 // Normal dispatch: one warp per token, persistent grid.
 struct DispatchArgs {
@@ -48,7 +60,7 @@ struct CombineArgs {
   const uint16_t* y;           // rows of bf16 [.][H]
   uint16_t* out;               // [T][H]
   long long y_rows;
-  int T, H, k, kmax;
+  int T, H, k, kmax, R;
   // normal mode
   const int2* dst;             // [T][kmax]
   const int* rank_offset;      // [R+1]
@@ -62,6 +74,42 @@ struct CombineArgs {
 void launch_combine(const CombineArgs& a, bool low_latency, int blocks, cudaStream_t stream);
 int combine_threads();
 const void* combine_kernel(bool low_latency);
+
+// TMA bulk-copy scatter (dispatch row movement), persistent: one block per SM.
+constexpr int kScatterMaxWarps = 8;
+constexpr int kScatterLoadsFp8 = 2;   // row loads in flight per warp (FP8)
+constexpr int kScatterQBufs = 2;      // quantised rows being stored per warp
+constexpr int kScatterLoadsBf16 = 3;  // row buffers per warp (BF16)
+struct ScatterArgs {
+  const uint16_t* x;           // [T][H] bf16
+  int T, H, k, kmax, El, R;
+  // normal destinations
+  const int2* dst;             // [T][kmax]
+  const int* rank_offset;      // [R+1]
+  long long cap;
+  const int* idx32;            // [T][k]
+  const float* topk_weights;   // [T][k] or null
+  int* recv_src_idx;
+  int* recv_topk_idx;
+  float* recv_topk_weights;
+  // low-latency destinations
+  const int* ll_idx;           // [T][k]
+  const int* ll_slot;          // [T][k]
+  int M;
+  int* recv_src_info;
+  // outputs
+  void* recv_x;
+  float* recv_scales;
+  int* err;
+};
+size_t scatter_smem_bytes(int H, int R, bool fp8, bool low_latency, int warps);
+int scatter_warps_for(int H, int R, bool fp8, bool low_latency, size_t smem_limit);
+cudaError_t configure_scatter(size_t smem_limit);
+void launch_scatter(const ScatterArgs& a, bool fp8, bool low_latency, int blocks, int warps, cudaStream_t stream);
+
+// Low-latency routing only (slots, counts); the rows move with k_scatter.
+void launch_ll_route(const RouteParams& p, const LowLatencyOutPtrs& o, size_t smem, cudaStream_t stream);
+cudaError_t configure_ll_route(size_t smem);
 
 // Fused low-latency dispatch: routing phase + per-chunk scatter.
 struct LowLatencyOut {

@@ -74,6 +74,55 @@ __global__ void __launch_bounds__(kRouteThreads) k_ll_dispatch(RouteParams p, Lo
   }
 }
 
+// Routing only: the same ranking as k_ll_dispatch on larger chunks, writing
+// the slots and counts that k_scatter and the low-latency combine use.
+__global__ void __launch_bounds__(kRouteThreads) k_ll_route(RouteParams p, LowLatencyOutPtrs o) {
+  extern __shared__ int smem_raw[];
+  const int NK = p.E;
+  const int NI = p.CT << p.kp_log2;
+  const RouteSmem s = route_smem_carve(smem_raw, NK, NI, p.CT, p.kmax);
+  const RouteTicket tk = route_take_ticket(p, s);
+  const int c = tk.chunk;
+  const int src = c / p.cps;
+  const int ci = c - src * p.cps;
+  const int t0 = src * p.tpr + ci * p.CT;
+  const int ct = min(p.CT, p.tpr - ci * p.CT);
+
+  route_rank_chunk<false>(p, s, t0, ct, NK);
+  route_lookback(p, s, c, tk.epoch, NK);
+
+  const int kp = 1 << p.kp_log2;
+  const int ipw = route_items_per_warp(NI);
+  for (int i = threadIdx.x; i < NI; i += kRouteThreads) {
+    const int tl = i >> p.kp_log2;
+    const int j = i & (kp - 1);
+    if (tl >= ct || j >= p.k) continue;
+    const int t = t0 + tl;
+    const int e = s.item_e[i];
+    int slot = -1;
+    if (e >= 0) {
+      slot = s.excl[e] + s.cnt[(i / ipw) * NK + e] + s.item_le[i];
+      if (slot >= o.M) {
+        latch_error(p.err, kErrCapacity);
+        slot = -1;
+      }
+    }
+    o.ll_idx[static_cast<size_t>(t) * p.k + j] = e;
+    o.ll_slot[static_cast<size_t>(t) * p.k + j] = slot;
+  }
+  if (c == p.C - 1 && o.recv_count) {
+    for (int e = threadIdx.x; e < p.E; e += kRouteThreads) o.recv_count[e] = min(s.excl[e] + s.agg[e], o.M);
+  }
+}
+
+void launch_ll_route(const RouteParams& p, const LowLatencyOutPtrs& o, size_t smem, cudaStream_t stream) {
+  k_ll_route<<<p.C, kRouteThreads, smem, stream>>>(p, o);
+}
+
+cudaError_t configure_ll_route(size_t smem) {
+  return cudaFuncSetAttribute(k_ll_route, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+}
+
 void launch_ll_dispatch(const RouteParams& p, const LowLatencyOut& o, bool fp8, size_t smem,
                         cudaStream_t stream) {
   if (fp8)

@@ -94,6 +94,11 @@ __device__ __forceinline__ int route_items_per_warp(int NI) {
   return (per + 31) & ~31;
 }
 
+// Items per chunk are at most kRouteMaxItems, so a warp holds at most
+// kRouteMaxBatches batches of 32 and can load all of its ids up front.
+constexpr int kRouteMaxItems = 2048;
+constexpr int kRouteMaxBatches = kRouteMaxItems / kRouteThreads;
+
 // Phase 1: chunk-local ranking.  kRanks adds the rank columns (layout).
 // Column layout: kRanks ? [R rank columns | E expert columns] : [E expert columns].
 template <bool kRanks>
@@ -103,6 +108,17 @@ __device__ inline void route_rank_chunk(const RouteParams& p, const RouteSmem& s
   const int NI = p.CT << p.kp_log2;
   const int ipw = route_items_per_warp(NI);
   const int colE = kRanks ? p.R : 0;
+  const int begin = warp * ipw;
+  const int end = min(NI, begin + ipw);
+  // every id this warp ranks, requested before any is used
+  long long pre[kRouteMaxBatches];
+#pragma unroll
+  for (int bb = 0; bb < kRouteMaxBatches; ++bb) {
+    const int i = begin + bb * 32 + lane;
+    const int tl = i >> p.kp_log2;
+    const int j = i & (kp - 1);
+    pre[bb] = (i < end && tl < ct && j < p.k) ? p.topk_idx[static_cast<long long>(t0 + tl) * p.k + j] : -1;
+  }
   for (int i = threadIdx.x; i < kRouteWarps * NK; i += kRouteThreads) s.cnt[i] = 0;
   __syncthreads();
 
@@ -110,22 +126,20 @@ __device__ inline void route_rank_chunk(const RouteParams& p, const RouteSmem& s
   const unsigned lt = lanemask_lt();
   const int gbase = lane & ~(kp - 1);
   const unsigned gmask = (kp == 32 ? kFullMask : ((1u << kp) - 1u)) << gbase;
-  const int begin = warp * ipw;
-  const int end = min(NI, begin + ipw);
-  for (int b = begin; b < end; b += 32) {  // warp-uniform
+#pragma unroll
+  for (int bb = 0; bb < kRouteMaxBatches; ++bb) {
+    const int b = begin + bb * 32;
+    if (b >= end) break;  // warp-uniform
     const int i = b + lane;
     const int tl = i >> p.kp_log2;
     const int j = i & (kp - 1);
     const bool in_chunk = i < end && tl < ct;
-    int e = -1;
-    if (in_chunk && j < p.k) {
-      long long v = p.topk_idx[static_cast<long long>(t0 + tl) * p.k + j];
-      if (v < -1 || v >= p.E) {
-        latch_error(p.err, kErrBadExpert);
-        v = -1;
-      }
-      e = static_cast<int>(v);
+    long long v = pre[bb];
+    if (v < -1 || v >= p.E) {
+      latch_error(p.err, kErrBadExpert);
+      v = -1;
     }
+    const int e = static_cast<int>(v);
     // expert columns: rank among this warp's entries for the same expert
     const unsigned pe = __match_any_sync(kFullMask, e);
     int le = 0;
@@ -181,6 +195,16 @@ __device__ inline void route_rank_chunk(const RouteParams& p, const RouteSmem& s
 
 // Phase 2: publish the chunk totals, then look back over earlier chunks for
 // each column's exclusive prefix, then publish the inclusive prefix.
+//
+// The look-back reads a window of kLookbackWindow predecessors with
+// independent loads and walks it from the nearest one, adding counts until it
+// meets an inclusive prefix.  Chunks publish at nearly the same moment, so
+// part of a window is often read just before it is written; the unread tail
+// of the window is then reloaded as a batch (one memory round trip per retry,
+// not one per predecessor).  Retries are bounded: after kSpinLimit the block
+// latches kErrTimeout and stops looking back.
+constexpr int kLookbackWindow = 32;
+
 __device__ inline void route_lookback(const RouteParams& p, const RouteSmem& s, int c, uint32_t epoch, int NK) {
   unsigned long long* mine = p.flags + static_cast<size_t>(c) * NK;
   for (int col = threadIdx.x; col < NK; col += kRouteThreads)
@@ -189,11 +213,40 @@ __device__ inline void route_lookback(const RouteParams& p, const RouteSmem& s, 
   for (int col = threadIdx.x; col < NK; col += kRouteThreads) {
     uint32_t ex = 0;
     if (c > 0) {
-      for (int q = c - 1; q >= 0; --q) {
-        const unsigned long long w =
-            flag_wait(p.flags + static_cast<size_t>(q) * NK + col, epoch, kFlagAggregate, p.err);
-        ex += flag_value(w);
-        if (flag_state(w) != kFlagAggregate) break;  // inclusive prefix found (or gave up)
+      bool done = false;
+      int retries = 0;
+      for (int q = c - 1; q >= 0 && !done; q -= kLookbackWindow) {
+        const int n = min(kLookbackWindow, q + 1);
+        unsigned long long w[kLookbackWindow];
+#pragma unroll
+        for (int j = 0; j < kLookbackWindow; ++j)
+          w[j] = j < n ? flag_load(p.flags + static_cast<size_t>(q - j) * NK + col) : 0ull;
+        int first = 0;  // entries before `first` are already added
+        while (true) {
+          int stale = -1;
+#pragma unroll
+          for (int j = 0; j < kLookbackWindow; ++j) {
+            if (j < first || j >= n || done || stale >= 0) continue;
+            const unsigned long long v = w[j];
+            if (flag_epoch(v) != epoch || flag_state(v) < kFlagAggregate) {
+              stale = j;
+            } else {
+              ex += flag_value(v);
+              if (flag_state(v) == kFlagInclusive) done = true;
+            }
+          }
+          if (done || stale < 0) break;
+          if (++retries > kSpinLimit) {
+            latch_error(p.err, kErrTimeout);
+            done = true;
+            break;
+          }
+          first = stale;
+          if (retries > 8) __nanosleep(32);
+#pragma unroll
+          for (int j = 0; j < kLookbackWindow; ++j)
+            if (j >= first && j < n) w[j] = flag_load(p.flags + static_cast<size_t>(q - j) * NK + col);
+        }
       }
       flag_store(mine + col, make_flag(epoch, kFlagInclusive, ex + static_cast<uint32_t>(s.agg[col])));
     }

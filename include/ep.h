@@ -169,8 +169,8 @@ ep_status_t ep_combine(ep_handle_t h, const void* y, int64_t y_rows, void* out, 
  *      recv_count   dev int32 [E] or NULL: rows filled per expert.
  * Rows past M (only possible with duplicated ids in one token) are skipped
  * and latch EP_ERR_CAPACITY.
- * num_sms is accepted for symmetry and not used: the kernel runs one block
- * per 8-token chunk, which at decode sizes is fewer blocks than SMs. */
+ * Two launches: a routing kernel (one block per chunk of 1024 (token, k)
+ * entries) and the row scatter, which occupies at most num_sms SMs (0 = all). */
 ep_status_t ep_low_latency_dispatch(ep_handle_t h, const void* x, const int64_t* topk_idx,
                                     int num_tokens, ep_dtype_t dtype, void* recv_x,
                                     float* recv_scales, int* recv_src_info, int* recv_count,

@@ -93,6 +93,7 @@ EDGE = [
     (2, 64, 32, 384, 40, 0.1, 0.0),    # top-32: a whole warp per token
     (8, 256, 8, 7168, 33, 0.01, 0.05), # V3 hidden, odd token count
     (5, 40, 4, 1024, 257, 0.3, 0.3),   # heavy masking and duplicates
+    (2, 4, 2, 40960, 4, 0.0, 0.0),     # rows too long for the bulk-copy staging: register kernels
 ]
 
 
@@ -121,6 +122,22 @@ def test_edge_shapes_all_steps(case):
         normal_path(R, E, k, H, idx, w, x, fp8=fp8, y=y, handle=h)
     for fp8 in (False, True):
         ll_path(R, E, k, H, idx, w, x, fp8=fp8, y_seed=5, handle=h)
+    h.close()
+
+
+@pytest.mark.parametrize("H", [512, 1024])
+def test_long_scatter_pipelines(H):
+    """Many tokens per warp, so every row buffer and barrier of the bulk-copy
+    scatter cycles several times (BF16 and FP8, normal and low latency)."""
+    R, E, k, tpr = 8, 64, 4, 2048
+    idx, w, x = _edge_inputs(R, E, k, H, tpr, 0.01, 0.05, seed=H)
+    L = oracle.layout(R, E, k, idx)
+    y = wl.normal_bf16(wl.rng(9), (int(L["rank_offset"][-1]), H))
+    h = ep.Handle(R, E, k, H, tpr)
+    for fp8 in (False, True):
+        normal_path(R, E, k, H, idx, w, x, fp8=fp8, y=y, handle=h)
+        normal_path(R, E, k, H, idx, w, x, fp8=fp8, handle=h, num_sms=7)
+        ll_path(R, E, k, H, idx, w, x, fp8=fp8, y_seed=3, handle=h)
     h.close()
 
 
