@@ -20,9 +20,10 @@ struct ep_handle {
   int layout_cmax, ll_cmax;
   // occupancy (blocks per SM) of the persistent kernels
   int occ_dispatch[2], occ_combine[2];
-  // TMA scatter: warps per block for [fp8][low_latency]; 0 = rows too long,
-  // the register-resident kernels are used instead
-  int scatter_warps[2][2];
+  // TMA scatter: row stages and consumer warps per block for
+  // [fp8][low_latency]; 0 stages = rows too long, the register-resident
+  // kernels are used instead
+  int scatter_ns[2][2], scatter_nc[2][2];
   size_t ll_route_smem;
   // state
   int T_layout;  // tokens of the last layout, -1 before the first
@@ -217,7 +218,7 @@ ep_status_t ep_handle_create(int R, int E, int k, int H, int max_tpr, ep_handle_
   h->ll_route_smem = ep::route_smem_bytes(NKll, h->layout_CT << lg, h->layout_CT, h->kmax);
   const size_t optin = static_cast<size_t>(prop.sharedMemPerBlockOptin);
   for (int f = 0; f < 2; ++f)
-    for (int l = 0; l < 2; ++l) h->scatter_warps[f][l] = ep::scatter_warps_for(H, R, f == 1, l == 1, optin);
+    for (int l = 0; l < 2; ++l) ep::scatter_config(H, R, f == 1, l == 1, optin, &h->scatter_ns[f][l], &h->scatter_nc[f][l]);
   if ((st = cuda_status(ep::configure_layout(h->layout_smem), "configure_layout")) != EP_OK ||
       (st = cuda_status(ep::configure_ll_dispatch(h->ll_smem), "configure_ll_dispatch")) != EP_OK ||
       (st = cuda_status(ep::configure_ll_route(h->ll_route_smem), "configure_ll_route")) != EP_OK ||
@@ -238,11 +239,11 @@ ep_status_t ep_handle_create(int R, int E, int k, int H, int max_tpr, ep_handle_
     std::fprintf(stderr,
                  "[ep] handle R=%d E=%d k=%d H=%d max_tokens_per_rank=%d on device %d (%d SMs); "
                  "layout chunk %d tokens (%zu B smem), ll chunk %d tokens (%zu B smem); "
-                 "blocks/SM dispatch bf16 %d fp8 %d, combine %d ll-combine %d; scatter warps bf16 %d fp8 %d; "
-                 "arena %zu B\n",
+                 "blocks/SM dispatch bf16 %d fp8 %d, combine %d ll-combine %d; scatter stages/consumers bf16 %d/%d "
+                 "fp8 %d/%d; arena %zu B\n",
                  R, E, k, H, max_tpr, h->device, h->num_sms, h->layout_CT, h->layout_smem, h->ll_CT,
                  h->ll_smem, h->occ_dispatch[0], h->occ_dispatch[1], h->occ_combine[0], h->occ_combine[1],
-                 h->scatter_warps[0][0], h->scatter_warps[1][0], off);
+                 h->scatter_ns[0][0], h->scatter_nc[0][0], h->scatter_ns[1][0], h->scatter_nc[1][0], off);
   *out = h;
   return EP_OK;
 }
@@ -335,8 +336,8 @@ ep_status_t ep_dispatch(ep_handle_t h, const void* x, const float* topk_weights,
   ep_status_t st = check_device(h);
   if (st != EP_OK) return st;
   if (T == 0) return EP_OK;
-  const int sw = h->scatter_warps[fp8 ? 1 : 0][0];
-  if (sw > 0) {
+  const int sns = h->scatter_ns[fp8 ? 1 : 0][0], snc = h->scatter_nc[fp8 ? 1 : 0][0];
+  if (sns > 0) {
     ep::ScatterArgs a{};
     a.x = static_cast<const uint16_t*>(x);
     a.T = T;
@@ -356,11 +357,11 @@ ep_status_t ep_dispatch(ep_handle_t h, const void* x, const float* topk_weights,
     a.recv_x = recv_x;
     a.recv_scales = recv_scales;
     a.err = h->err;
-    const int blocks = grid_for(h, 1, num_sms, T, sw);
-    ep::launch_scatter(a, fp8, false, blocks, sw, reinterpret_cast<cudaStream_t>(stream));
+    const int blocks = grid_for(h, 1, num_sms, T, 1);
+    ep::launch_scatter(a, fp8, false, blocks, sns, snc, reinterpret_cast<cudaStream_t>(stream));
     if (h->debug)
-      std::fprintf(stderr, "[ep] dispatch %s T=%d: TMA scatter %d blocks x %d warps\n", fp8 ? "fp8" : "bf16", T,
-                   blocks, sw);
+      std::fprintf(stderr, "[ep] dispatch %s T=%d: TMA scatter %d blocks, %d stages, %d consumers\n",
+                   fp8 ? "fp8" : "bf16", T, blocks, sns, snc);
     return cuda_status(cudaGetLastError(), "k_scatter launch");
   }
   ep::DispatchArgs a;
@@ -435,8 +436,8 @@ ep_status_t ep_low_latency_dispatch(ep_handle_t h, const void* x, const int64_t*
     if (recv_count) return cuda_status(cudaMemsetAsync(recv_count, 0, sizeof(int) * h->E, s), "ll memset");
     return EP_OK;
   }
-  const int sw = h->scatter_warps[fp8 ? 1 : 0][1];
-  if (sw > 0) {
+  const int sns = h->scatter_ns[fp8 ? 1 : 0][1], snc = h->scatter_nc[fp8 ? 1 : 0][1];
+  if (sns > 0) {
     // routing (slots, counts) on layout-sized chunks, then the TMA scatter
     RouteParams p = route_params(h, topk_idx, T, h->layout_CT, h->ll_flags, h->tickets + 1);
     ep::LowLatencyOutPtrs ro{recv_count, h->ll_idx, h->ll_slot, M};
@@ -457,12 +458,12 @@ ep_status_t ep_low_latency_dispatch(ep_handle_t h, const void* x, const int64_t*
     a.recv_x = recv_x;
     a.recv_scales = recv_scales;
     a.err = h->err;
-    const int blocks = grid_for(h, 1, num_sms, T, sw);
-    ep::launch_scatter(a, fp8, true, blocks, sw, s);
+    const int blocks = grid_for(h, 1, num_sms, T, 1);
+    ep::launch_scatter(a, fp8, true, blocks, sns, snc, s);
     if ((st = cuda_status(cudaGetLastError(), "k_scatter(ll) launch")) != EP_OK) return st;
     if (h->debug)
-      std::fprintf(stderr, "[ep] ll dispatch T=%d: route %d blocks, TMA scatter %d blocks x %d warps\n", T, p.C,
-                   blocks, sw);
+      std::fprintf(stderr, "[ep] ll dispatch T=%d: route %d blocks, TMA scatter %d blocks, %d stages, %d consumers\n",
+                   T, p.C, blocks, sns, snc);
     h->T_ll = T;
     return EP_OK;
   }

@@ -147,9 +147,9 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine(CombineArgs a) {
 
 void launch_combine(const CombineArgs& a, bool low_latency, int blocks, cudaStream_t stream) {
   if (low_latency)
-    k_combine<true><<<blocks, kCombineThreads, 0, stream>>>(a);
+    (void)launch_kernel(k_combine<true>, dim3(blocks), dim3(kCombineThreads), 0, stream, a);
   else
-    k_combine<false><<<blocks, kCombineThreads, 0, stream>>>(a);
+    (void)launch_kernel(k_combine<false>, dim3(blocks), dim3(kCombineThreads), 0, stream, a);
 }
 
 int combine_threads() { return kCombineThreads; }

@@ -66,9 +66,9 @@ __global__ void __launch_bounds__(kDispatchThreads, 2) k_dispatch(DispatchArgs a
 
 void launch_dispatch(const DispatchArgs& a, bool fp8, int blocks, cudaStream_t stream) {
   if (fp8)
-    k_dispatch<true><<<blocks, kDispatchThreads, 0, stream>>>(a);
+    (void)launch_kernel(k_dispatch<true>, dim3(blocks), dim3(kDispatchThreads), 0, stream, a);
   else
-    k_dispatch<false><<<blocks, kDispatchThreads, 0, stream>>>(a);
+    (void)launch_kernel(k_dispatch<false>, dim3(blocks), dim3(kDispatchThreads), 0, stream, a);
 }
 
 int dispatch_threads() { return kDispatchThreads; }

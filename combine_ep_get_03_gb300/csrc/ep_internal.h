@@ -5,7 +5,21 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace ep {
+
+// Kernel launch through cudaLaunchKernelEx (one code path for every kernel).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                 Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 struct RouteParams;  // routing.cuh
 
@@ -75,11 +89,9 @@ void launch_combine(const CombineArgs& a, bool low_latency, int blocks, cudaStre
 int combine_threads();
 const void* combine_kernel(bool low_latency);
 
-// TMA bulk-copy scatter (dispatch row movement), persistent: one block per SM.
-constexpr int kScatterMaxWarps = 8;
-constexpr int kScatterLoadsFp8 = 2;   // row loads in flight per warp (FP8)
-constexpr int kScatterQBufs = 2;      // quantised rows being stored per warp
-constexpr int kScatterLoadsBf16 = 3;  // row buffers per warp (BF16)
+// TMA bulk-copy scatter (dispatch row movement), persistent: one block per
+// SM, one producer warp and up to kScatterMaxConsumers consumer warps.
+constexpr int kScatterMaxConsumers = 8;
 struct ScatterArgs {
   const uint16_t* x;           // [T][H] bf16
   int T, H, k, kmax, El, R;
@@ -102,10 +114,13 @@ struct ScatterArgs {
   float* recv_scales;
   int* err;
 };
-size_t scatter_smem_bytes(int H, int R, bool fp8, bool low_latency, int warps);
-int scatter_warps_for(int H, int R, bool fp8, bool low_latency, size_t smem_limit);
+// NS row stages and NC consumer warps that fit `smem_limit` (NS = 0: the
+// rows are too long for the bulk-copy staging).
+void scatter_config(int H, int R, bool fp8, bool low_latency, size_t smem_limit, int* NS, int* NC);
+size_t scatter_smem_bytes(int H, int R, bool fp8, bool low_latency, int NS, int NC);
 cudaError_t configure_scatter(size_t smem_limit);
-void launch_scatter(const ScatterArgs& a, bool fp8, bool low_latency, int blocks, int warps, cudaStream_t stream);
+void launch_scatter(const ScatterArgs& a, bool fp8, bool low_latency, int blocks, int NS, int NC,
+                    cudaStream_t stream);
 
 // Low-latency routing only (slots, counts); the rows move with k_scatter.
 void launch_ll_route(const RouteParams& p, const LowLatencyOutPtrs& o, size_t smem, cudaStream_t stream);

@@ -305,7 +305,7 @@ void launch_layout_tokens(const RouteParams& p, const LayoutOutPtrs& out, cudaSt
   o.num_tokens_per_expert = out.num_tokens_per_expert;
   o.is_token_in_rank = out.is_token_in_rank;
   const size_t smem = layout_tokens_smem_bytes(p.R, p.E, p.CT, p.kmax);
-  k_layout_tokens<<<p.C, kRouteThreads, smem, stream>>>(p, o);
+  (void)launch_kernel(k_layout_tokens, dim3(p.C), dim3(kRouteThreads), smem, stream, p, o);
 }
 
 size_t layout_tokens_smem(int R, int E, int CT, int kmax) { return layout_tokens_smem_bytes(R, E, CT, kmax); }
@@ -324,7 +324,7 @@ void launch_layout(const RouteParams& p, const LayoutOutPtrs& out, size_t smem, 
   o.num_tokens_per_rank = out.num_tokens_per_rank;
   o.num_tokens_per_expert = out.num_tokens_per_expert;
   o.is_token_in_rank = out.is_token_in_rank;
-  k_layout<<<p.C, kRouteThreads, smem, stream>>>(p, o);
+  (void)launch_kernel(k_layout, dim3(p.C), dim3(kRouteThreads), smem, stream, p, o);
 }
 
 cudaError_t configure_layout(size_t smem) {

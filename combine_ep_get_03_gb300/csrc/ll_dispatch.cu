@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(kRouteThreads) k_ll_route(RouteParams p, LowLa
 }
 
 void launch_ll_route(const RouteParams& p, const LowLatencyOutPtrs& o, size_t smem, cudaStream_t stream) {
-  k_ll_route<<<p.C, kRouteThreads, smem, stream>>>(p, o);
+  (void)launch_kernel(k_ll_route, dim3(p.C), dim3(kRouteThreads), smem, stream, p, o);
 }
 
 cudaError_t configure_ll_route(size_t smem) {
@@ -126,9 +126,9 @@ cudaError_t configure_ll_route(size_t smem) {
 void launch_ll_dispatch(const RouteParams& p, const LowLatencyOut& o, bool fp8, size_t smem,
                         cudaStream_t stream) {
   if (fp8)
-    k_ll_dispatch<true><<<p.C, kRouteThreads, smem, stream>>>(p, o);
+    (void)launch_kernel(k_ll_dispatch<true>, dim3(p.C), dim3(kRouteThreads), smem, stream, p, o);
   else
-    k_ll_dispatch<false><<<p.C, kRouteThreads, smem, stream>>>(p, o);
+    (void)launch_kernel(k_ll_dispatch<false>, dim3(p.C), dim3(kRouteThreads), smem, stream, p, o);
 }
 
 cudaError_t configure_ll_dispatch(size_t smem) {

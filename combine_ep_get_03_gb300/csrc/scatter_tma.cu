@@ -1,14 +1,14 @@
-// Dispatch's row movement on sm_103a with TMA bulk copies: each warp streams
-// its tokens through shared memory -- a bulk load brings a token row in, the
-// warp quantises it once to FP8 (or leaves BF16 as is), and one bulk store per
-// destination writes it out ("DeepEP 要約" (stakiran.github.io) section 3:
-// dispatch and low_latency_dispatch; "DeepSeek выпустила DeepEP V2.5"
-// (aikraft.ru), "Технические детали и требования": FP8 dispatch).
+// Dispatch's row movement on sm_103a with TMA bulk copies ("DeepEP 要約"
+// (stakiran.github.io) section 3: dispatch and low_latency_dispatch;
+// "DeepSeek выпустила DeepEP V2.5" (aikraft.ru), "Технические детали и
+// требования": FP8 dispatch).  A token row is read from HBM once by a bulk
+// load into shared memory, quantised once to FP8 (or kept as BF16), and
+// written to each destination by one bulk store per destination.
 //
-// HBM-bound: the row is read once (2H bytes) and written once per
-// destination.  The bytes in flight are bounded by shared memory, not by
-// registers: every warp keeps its next rows' loads in flight while it
-// quantises and stores the current one.
+// HBM-bound.  One persistent block per SM: a producer warp keeps up to NS row
+// loads in flight through a ring of stages, and NC consumer warps quantise
+// and store, so both the bytes in flight and the quantisation warps are
+// bounded by shared memory rather than registers.
 //
 // Destinations:  normal  -- the handle's (rank, row-in-rank) list + the
 //                           rank's region offset (the layout's output);
@@ -21,21 +21,6 @@
 #include "ep_internal.h"
 
 namespace ep {
-
-// Each warp's region starts with its mbarriers (8 bytes each), padded to 16.
-constexpr size_t kScatterBarBytes = 32;
-static_assert(8 * kScatterLoadsFp8 <= kScatterBarBytes && 8 * kScatterLoadsBf16 <= kScatterBarBytes,
-              "every row buffer needs its own mbarrier inside the warp's barrier area");
-
-__host__ __device__ inline size_t scatter_warp_bytes(int H, bool fp8) {
-  const size_t G = static_cast<size_t>(H) / 128;
-  if (fp8)
-    return kScatterBarBytes + kScatterLoadsFp8 * 2 * static_cast<size_t>(H) +
-           kScatterQBufs * (H + ((4 * G + 15) & ~15ull));
-  return kScatterBarBytes + kScatterLoadsBf16 * 2 * static_cast<size_t>(H);
-}
-
-__host__ __device__ inline size_t scatter_head_bytes(int R) { return (static_cast<size_t>(R + 1) * 4 + 15) & ~15ull; }
 
 // Largest |x| of 8 bf16 values, accumulated in packed form: with the sign
 // bits cleared, bf16 values compare like their bit patterns, and max.bf16x2
@@ -99,51 +84,75 @@ __device__ __forceinline__ void quantize_row_smem(const unsigned char* x, unsign
   }
 }
 
+// Block layout (dynamic shared memory):
+//   [rank_offset: R+1 ints, normal mode][full[NS], empty[NS] mbarriers]
+//   [NS row stages of 2H bytes][NC quantised-row buffers of H + scales (FP8)]
+// Warp 0 is the producer: lane 0 streams the block's token rows into the
+// stages with bulk loads (full[s] counts the bytes).  Warps 1..NC are
+// consumers: consumer c takes the block's tokens c, c+NC, ...; it waits for
+// its stage, quantises it into its own buffer (FP8) or stores straight from
+// the stage (BF16), releases the stage (empty[s]) once nothing reads it any
+// more, and bulk-stores the row to every destination.
+__host__ __device__ inline size_t scatter_head_bytes(int R) { return (static_cast<size_t>(R + 1) * 4 + 15) & ~15ull; }
+__host__ __device__ inline size_t scatter_qbuf_bytes(int H) {
+  return static_cast<size_t>(H) + ((4 * static_cast<size_t>(H / 128) + 15) & ~15ull);
+}
+__host__ __device__ inline size_t scatter_block_bytes(int H, int R, bool fp8, bool low_latency, int NS, int NC) {
+  return scatter_head_bytes(low_latency ? 0 : R) + 16 * static_cast<size_t>(NS) +
+         static_cast<size_t>(NS) * 2 * static_cast<size_t>(H) + (fp8 ? static_cast<size_t>(NC) * scatter_qbuf_bytes(H) : 0);
+}
+
 template <bool kFP8, bool kLL>
-__global__ void __launch_bounds__(kScatterMaxWarps * 32, 1) k_scatter(ScatterArgs a) {
+__global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_scatter(ScatterArgs a, int NS) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const int nw = blockDim.x >> 5;
-  int* so = reinterpret_cast<int*>(smem);  // rank_offset (normal mode)
-  if (!kLL) {
-    for (int r = threadIdx.x; r <= a.R; r += blockDim.x) so[r] = a.rank_offset[r];
-    __syncthreads();
-  }
-  constexpr int NB = kFP8 ? kScatterLoadsFp8 : kScatterLoadsBf16;
+  const int NC = (blockDim.x >> 5) - 1;
   const int H = a.H;
   const int G = H >> 7;
   const uint32_t row_bytes = 2u * static_cast<uint32_t>(H);
-  unsigned char* wb = smem + scatter_head_bytes(kLL ? 0 : a.R) + static_cast<size_t>(warp) * scatter_warp_bytes(H, kFP8);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(wb);
-  unsigned char* xb0 = wb + kScatterBarBytes;
-  unsigned char* qb0 = xb0 + static_cast<size_t>(NB) * row_bytes;
-  const size_t qstride = static_cast<size_t>(H) + ((4 * G + 15) & ~15);
-  auto xb = [&](int b) { return xb0 + static_cast<size_t>(b) * row_bytes; };
-  auto qb = [&](int q) { return qb0 + static_cast<size_t>(q) * qstride; };
-  auto sc = [&](int q) { return reinterpret_cast<float*>(qb(q) + H); };
+  int* so = reinterpret_cast<int*>(smem);  // rank_offset (normal mode)
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + scatter_head_bytes(kLL ? 0 : a.R));
+  uint64_t* empty = full + NS;
+  unsigned char* stage0 = reinterpret_cast<unsigned char*>(empty + NS);
+  unsigned char* qbuf0 = stage0 + static_cast<size_t>(NS) * row_bytes;
+  auto stage = [&](int s) { return stage0 + static_cast<size_t>(s) * row_bytes; };
 
-  const int gw = blockIdx.x * nw + warp;
-  const int total = gridDim.x * nw;
-  const int n_my = gw < a.T ? (a.T - gw + total - 1) / total : 0;
-  if (lane == 0) {
-    for (int b = 0; b < NB; ++b) mbar_init(bar + b, 1);
+  if (!kLL)
+    for (int r = threadIdx.x; r <= a.R; r += blockDim.x) so[r] = a.rank_offset[r];
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
     mbar_init_fence();
   }
-  __syncwarp();
-  auto issue_load = [&](int i, int b) {  // lane 0 only
-    const int t = gw + i * total;
-    mbar_arrive_expect_tx(bar + b, row_bytes);
-    bulk_load(xb(b), a.x + static_cast<size_t>(t) * H, row_bytes, bar + b);
-  };
-  constexpr int ahead = kFP8 ? NB : NB - 1;
-  if (lane == 0)
-    for (int i = 0; i < ahead && i < n_my; ++i) issue_load(i, i);
+  __syncthreads();
+  // this block's tokens: blockIdx.x + i * gridDim.x
+  const int n_blk = static_cast<int>(blockIdx.x) < a.T ? (a.T - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x : 0;
 
+  if (warp == 0) {
+    // producer
+    if (lane == 0) {
+      for (int i = 0; i < n_blk; ++i) {
+        const int s = i % NS;
+        if (i >= NS && !mbar_wait(empty + s, static_cast<uint32_t>((i / NS - 1) & 1), a.err)) break;
+        const int t = blockIdx.x + i * gridDim.x;
+        mbar_arrive_expect_tx(full + s, row_bytes);
+        bulk_load(stage(s), a.x + static_cast<size_t>(t) * H, row_bytes, full + s);
+      }
+    }
+    return;
+  }
+
+  const int cc = warp - 1;  // consumer index
+  unsigned char* qd = qbuf0 + static_cast<size_t>(cc) * scatter_qbuf_bytes(H);
+  float* sd = reinterpret_cast<float*>(qd + H);
   const bool meta = !kLL && (a.recv_src_idx || a.recv_topk_idx || a.recv_topk_weights);
-  for (int i = 0; i < n_my; ++i) {
-    const int t = gw + i * total;
-    const int b = i % NB;
+  bool first = true;
+  for (int i = cc; i < n_blk; i += NC) {
+    const int t = blockIdx.x + i * gridDim.x;
+    const int s = i % NS;
     // destinations of this token (overlaps the row load)
     long long row = -1;
     int r = -1, e = -1;
@@ -170,50 +179,43 @@ __global__ void __launch_bounds__(kScatterMaxWarps * 32, 1) k_scatter(ScatterArg
       if (ee >= 0 && ss >= 0) row = static_cast<long long>(ee) * a.M + ss;
     }
     const unsigned dmask = __ballot_sync(kFullMask, row >= 0);
-    const bool landed = mbar_wait(bar + b, static_cast<uint32_t>((i / NB) & 1), a.err);
-    if (!__all_sync(kFullMask, landed)) break;  // gave up (latched): stop this warp's tokens
+    const bool landed = mbar_wait(full + s, static_cast<uint32_t>((i / NS) & 1), a.err);
+    if (!__all_sync(kFullMask, landed)) break;  // gave up (latched)
 
-    const unsigned char* src;
     if (kFP8) {
-      const int q = i % kScatterQBufs;
-      if (i >= kScatterQBufs) {
-        if (lane == 0) bulk_wait_read<kScatterQBufs - 1>();  // qb(q)'s previous stores have read it
+      if (!first) {
+        if (lane == 0) bulk_wait_read<0>();  // this consumer's previous stores have read its buffer
         __syncwarp();
       }
-      unsigned char* qd = qb(q);
-      float* sd = sc(q);
-      quantize_row_smem(xb(b), qd, sd, G, lane);
+      quantize_row_smem(stage(s), qd, sd, G, lane);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0 && i + NB < n_my) issue_load(i + NB, b);  // the row buffer is free again
-      src = qd;
+      if (lane == 0) mbar_arrive(empty + s);  // the stage is free again
       unsigned m = dmask;
       while (m) {
         const int sl = __ffs(m) - 1;
         m &= m - 1;
         const long long rr = __shfl_sync(kFullMask, row, sl);
-        if (lane == 0) bulk_store(static_cast<uint8_t*>(a.recv_x) + rr * H, src, static_cast<uint32_t>(H));
+        if (lane == 0) bulk_store(static_cast<uint8_t*>(a.recv_x) + rr * H, qd, static_cast<uint32_t>(H));
         for (int g = lane; g < G; g += 32) a.recv_scales[rr * G + g] = sd[g];
       }
       if (lane == 0) bulk_commit();
     } else {
-      src = xb(b);
       unsigned m = dmask;
       while (m) {
         const int sl = __ffs(m) - 1;
         m &= m - 1;
         const long long rr = __shfl_sync(kFullMask, row, sl);
-        if (lane == 0) bulk_store(static_cast<uint16_t*>(a.recv_x) + rr * H, src, row_bytes);
+        if (lane == 0) bulk_store(static_cast<uint16_t*>(a.recv_x) + rr * H, stage(s), row_bytes);
       }
       if (lane == 0) {
         bulk_commit();
-        if (i + NB - 1 < n_my) {
-          bulk_wait_read<1>();  // token i-1's stores have read the buffer reloaded next
-          issue_load(i + NB - 1, (i + NB - 1) % NB);
-        }
+        bulk_wait_read<0>();  // the stores have read the stage
+        mbar_arrive(empty + s);
       }
       __syncwarp();
     }
+    first = false;
     // per-row metadata
     if (meta) {
       unsigned m = dmask;
@@ -237,14 +239,28 @@ __global__ void __launch_bounds__(kScatterMaxWarps * 32, 1) k_scatter(ScatterArg
   __syncwarp();
 }
 
-size_t scatter_smem_bytes(int H, int R, bool fp8, bool low_latency, int warps) {
-  return scatter_head_bytes(low_latency ? 0 : R) + static_cast<size_t>(warps) * scatter_warp_bytes(H, fp8);
+// Consumers and stages for a block: FP8 wants compute warps (8 consumers, the
+// rest of shared memory as stages); BF16 only moves bytes (4 consumers, more
+// stages).  Fewer consumers if the rows are long; 0 if not even two stages fit.
+void scatter_config(int H, int R, bool fp8, bool low_latency, size_t smem_limit, int* NS, int* NC) {
+  *NS = 0;
+  *NC = 0;
+  for (int nc = fp8 ? kScatterMaxConsumers : 4; nc >= 1; --nc) {
+    const size_t fixed = scatter_block_bytes(H, R, fp8, low_latency, 0, nc);
+    if (fixed >= smem_limit) continue;
+    const size_t per_stage = 16 + 2 * static_cast<size_t>(H);
+    int ns = static_cast<int>((smem_limit - fixed) / per_stage);
+    if (ns > 32) ns = 32;
+    if (ns >= 2) {
+      *NS = ns;
+      *NC = nc;
+      return;
+    }
+  }
 }
 
-int scatter_warps_for(int H, int R, bool fp8, bool low_latency, size_t smem_limit) {
-  int w = kScatterMaxWarps;
-  while (w > 0 && scatter_smem_bytes(H, R, fp8, low_latency, w) > smem_limit) --w;
-  return w;
+size_t scatter_smem_bytes(int H, int R, bool fp8, bool low_latency, int NS, int NC) {
+  return scatter_block_bytes(H, R, fp8, low_latency, NS, NC);
 }
 
 cudaError_t configure_scatter(size_t smem_limit) {
@@ -259,19 +275,20 @@ cudaError_t configure_scatter(size_t smem_limit) {
   return cudaSuccess;
 }
 
-void launch_scatter(const ScatterArgs& a, bool fp8, bool low_latency, int blocks, int warps, cudaStream_t stream) {
-  const size_t smem = scatter_smem_bytes(a.H, a.R, fp8, low_latency, warps);
-  const dim3 grid(blocks), block(warps * 32);
+void launch_scatter(const ScatterArgs& a, bool fp8, bool low_latency, int blocks, int NS, int NC,
+                    cudaStream_t stream) {
+  const size_t smem = scatter_block_bytes(a.H, a.R, fp8, low_latency, NS, NC);
+  const dim3 grid(blocks), block((NC + 1) * 32);
   if (low_latency) {
     if (fp8)
-      k_scatter<true, true><<<grid, block, smem, stream>>>(a);
+      (void)launch_kernel(k_scatter<true, true>, grid, block, smem, stream, a, NS);
     else
-      k_scatter<false, true><<<grid, block, smem, stream>>>(a);
+      (void)launch_kernel(k_scatter<false, true>, grid, block, smem, stream, a, NS);
   } else {
     if (fp8)
-      k_scatter<true, false><<<grid, block, smem, stream>>>(a);
+      (void)launch_kernel(k_scatter<true, false>, grid, block, smem, stream, a, NS);
     else
-      k_scatter<false, false><<<grid, block, smem, stream>>>(a);
+      (void)launch_kernel(k_scatter<false, false>, grid, block, smem, stream, a, NS);
   }
 }
 
