@@ -61,8 +61,13 @@ def _load():
             lib.ref_combine.argtypes = [I, I, I, I, I, P, P, I64, P]
             lib.ref_ll_dispatch.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P]
             lib.ref_ll_combine.argtypes = [I, I, I, I, I, I, P, P, P, P]
+            lib.ref_combine_ex.argtypes = [I, I, I, I, I, P, I, P, P, I64, P, P, P]
+            lib.ref_em_layout.argtypes = [I, I, I, I, P, I, P, P, P]
+            lib.ref_em_dispatch.argtypes = [I, I, I, I, I, I, P, P, P, I, I64, P, P, I64, P, P]
+            lib.ref_em_combine.argtypes = [I, I, I, I, I, P, I, P, I64, P]
             for name in ("ref_quantize_row", "ref_layout", "ref_dispatch", "ref_combine",
-                         "ref_ll_dispatch", "ref_ll_combine"):
+                         "ref_ll_dispatch", "ref_ll_combine", "ref_combine_ex", "ref_em_layout",
+                         "ref_em_dispatch", "ref_em_combine"):
                 getattr(lib, name).restype = I
             _lib = lib
     return _lib
@@ -208,4 +213,75 @@ def ll_combine(R, E, k, M, topk_idx, topk_weights, y_bits):
     H = y_bits.shape[-1]
     out = np.zeros((T, H), np.uint16)
     _check(_load().ref_ll_combine(R, E, k, T, H, M, _p(idx), _p(w), _p(y_bits), _p(out)))
+    return out
+
+
+def combine_ex(R, E, k, topk_idx, y, y_scales=None, recv_topk_weights=None):
+    """Normal combine, general form.  y is uint16 bf16 bits [rows, H], or
+    uint8 e4m3 bytes [rows, H] with fp32 y_scales [rows, H/128].  With
+    recv_topk_weights [rows, k] the weights are summed back too.  Returns
+    (out uint16 [T, H], combined weights float32 [T, k] or None)."""
+    idx = _c(topk_idx, np.int64)
+    fp8 = y_scales is not None
+    y = _c(y, np.uint8 if fp8 else np.uint16)
+    sc = None if y_scales is None else _c(y_scales, np.float32)
+    rw = None if recv_topk_weights is None else _c(recv_topk_weights, np.float32)
+    T = idx.shape[0]
+    H = y.shape[1]
+    out = np.zeros((T, H), np.uint16)
+    cw = None if rw is None else np.zeros((T, k), np.float32)
+    _check(_load().ref_combine_ex(R, E, k, T, H, _p(idx), int(fp8), _p(y), _p(sc), y.shape[0], _p(rw),
+                                  _p(out), _p(cw)))
+    return out, cw
+
+
+def em_layout(R, E, k, topk_idx, align):
+    """Expert-major layout: dict(num_recv_per_expert [E], expert_offset [E+1],
+    row [T, k])."""
+    idx = _c(topk_idx, np.int64)
+    T = idx.shape[0]
+    out = dict(num_recv_per_expert=np.zeros(E, np.int32), expert_offset=np.zeros(E + 1, np.int32),
+               row=np.zeros((T, k), np.int32))
+    _check(_load().ref_em_layout(R, E, k, T, _p(idx), int(align), _p(out["num_recv_per_expert"]),
+                                 _p(out["expert_offset"]), _p(out["row"])))
+    return out
+
+
+def em_dispatch(R, E, k, x_bits, topk_idx, topk_weights, fp8, align, capacity_rows=None, scales_ld=None):
+    """Expert-major dispatch.  Returns (dict, status); recv_scales is
+    group-major [H/128, scales_ld]; rows the oracle does not write keep the
+    fill values (recv_x 0, scales -7, src_idx -7, weights -7)."""
+    x_bits = _c(x_bits, np.uint16)
+    idx = _c(topk_idx, np.int64)
+    T, H = x_bits.shape
+    if capacity_rows is None:
+        capacity_rows = int(em_layout(R, E, k, idx, align)["expert_offset"][-1])
+    if scales_ld is None:
+        scales_ld = (int(capacity_rows) + 3) // 4 * 4
+    rows = max(int(capacity_rows), 1)
+    w = None if topk_weights is None else _c(topk_weights, np.float32)
+    out = dict(
+        recv_x=np.zeros((rows, H), np.uint8 if fp8 else np.uint16),
+        recv_scales=np.full((H // 128, max(scales_ld, 1)), -7.0, np.float32) if fp8 else None,
+        recv_src_idx=np.full(rows, -7, np.int32),
+        recv_weights=np.full(rows, -7.0, np.float32),
+    )
+    st = _check(_load().ref_em_dispatch(R, E, k, T, H, int(bool(fp8)), _p(x_bits), _p(idx), _p(w), int(align),
+                                        int(capacity_rows), _p(out["recv_x"]), _p(out["recv_scales"]),
+                                        int(scales_ld), _p(out["recv_src_idx"]), _p(out["recv_weights"])),
+                allow=(OK, CAPACITY))
+    if capacity_rows == 0:
+        for key in ("recv_x", "recv_src_idx", "recv_weights"):
+            out[key] = out[key][:0]
+    return out, st
+
+
+def em_combine(R, E, k, topk_idx, align, y_bits):
+    """Expert-major combine: y (uint16 [rows, H]) -> out (uint16 [T, H])."""
+    idx = _c(topk_idx, np.int64)
+    y_bits = _c(y_bits, np.uint16)
+    T = idx.shape[0]
+    H = y_bits.shape[1]
+    out = np.zeros((T, H), np.uint16)
+    _check(_load().ref_em_combine(R, E, k, T, H, _p(idx), int(align), _p(y_bits), y_bits.shape[0], _p(out)))
     return out

@@ -39,7 +39,19 @@
 //  (5) low-latency slots are handed out in (source rank, token, k-index)
 //      order; low-latency combine is acc = fmaf(w, y, acc) over the token's
 //      entries in ascending expert id (k-index breaks ties), from +0.0f;
-//  (6) an id of -1 is a masked entry; any other id outside [0, E) is an error.
+//  (6) an id of -1 is a masked entry; any other id outside [0, E) is an error;
+//  (7) an e4m3 combine input is dequantised as decode(q) * scale (one RN
+//      multiply, the scale of the row's 128-channel group) before the sum;
+//      combine can also sum the receive-side per-row top-k weights back to
+//      the source token, column by column, in the same ascending rank order;
+//  (8) the expert-major ("GEMM") receive layout has one row per unmasked
+//      (token, k-index) entry, grouped by ascending expert id, each expert's
+//      group starting at a multiple of `align` rows; inside a group the
+//      entries keep (source rank, token, k-index) order.  Its fp8 scales are
+//      stored group-major, scales[g * ld + row], so that one group's scales
+//      of consecutive rows are contiguous.  Its combine is the unweighted
+//      fp32 sum of the token's rows in ascending expert id (k-index breaks
+//      ties), from +0.0f.
 //
 // Compile with floating-point contraction off (-ffp-contract=off): every
 // multiply and add below is meant as one IEEE-754 binary32 operation.
@@ -254,6 +266,42 @@ bool ll_slots(const Shape& s, const int64_t* topk_idx, int M, std::vector<int>* 
   return overflow;
 }
 
+// Value of channel h of receive row `row` as fp32: a bf16 row widens
+// exactly; an e4m3 row is decoded and multiplied by its group's scale.
+float combine_input(int y_fp8, const void* y, const float* y_scales, int H, int64_t row, int h) {
+  if (!y_fp8) return bf16_bits_to_float(static_cast<const uint16_t*>(y)[row * H + h]);
+  float code_value = e4m3_to_float(static_cast<const uint8_t*>(y)[row * H + h]);
+  return code_value * y_scales[row * (H / 128) + h / 128];  // one RN multiply
+}
+
+// Expert-major rows.  count[e] = entries routed to e; offset[e] = first row
+// of expert e's group (each group rounded up to a multiple of align rows);
+// row[t * k + j] = row of entry (t, j), or -1 if masked.  Entries are visited
+// in (token, k-index) order, which is (source rank, token, k-index) order.
+void em_rows(const Shape& s, const int64_t* topk_idx, int align, std::vector<int>* count,
+             std::vector<int>* offset, std::vector<int>* row) {
+  count->assign(s.E, 0);
+  std::vector<int> rank_in_expert(static_cast<size_t>(s.T) * s.k, -1);
+  for (int t = 0; t < s.T; ++t)
+    for (int j = 0; j < s.k; ++j) {
+      int64_t e = topk_idx[static_cast<size_t>(t) * s.k + j];
+      if (e < 0) continue;
+      rank_in_expert[static_cast<size_t>(t) * s.k + j] = (*count)[e];
+      (*count)[e] += 1;
+    }
+  offset->assign(s.E + 1, 0);
+  for (int e = 0; e < s.E; ++e) {
+    int padded = ((*count)[e] + align - 1) / align * align;
+    (*offset)[e + 1] = (*offset)[e] + padded;
+  }
+  row->assign(static_cast<size_t>(s.T) * s.k, -1);
+  for (int t = 0; t < s.T; ++t)
+    for (int j = 0; j < s.k; ++j) {
+      size_t i = static_cast<size_t>(t) * s.k + j;
+      if (rank_in_expert[i] >= 0) (*row)[i] = (*offset)[topk_idx[i]] + rank_in_expert[i];
+    }
+}
+
 }  // namespace
 
 extern "C" {
@@ -333,28 +381,46 @@ int ref_dispatch(int R, int E, int k, int T, int H, int fp8, const uint16_t* x,
   return overflow ? kCapacity : kOk;
 }
 
-int ref_combine(int R, int E, int k, int T, int H, const int64_t* topk_idx, const uint16_t* y,
-                int64_t y_rows, uint16_t* out) {
+int ref_combine_ex(int R, int E, int k, int T, int H, const int64_t* topk_idx, int y_fp8, const void* y,
+                   const float* y_scales, int64_t y_rows, const float* recv_topk_weights, uint16_t* out,
+                   float* combined_topk_weights) {
   Shape s;
   int st = check_shape(R, E, k, T, &s);
   if (st != kOk) return st;
-  if (H <= 0 || H % 128 != 0) return kInvalidArg;
+  if (H <= 0 || H % 128 != 0 || (y_fp8 && !y_scales)) return kInvalidArg;
   if ((st = check_ids(s, topk_idx)) != kOk) return st;
   Layout L;
   compute_layout(s, topk_idx, &L);
   if (L.rank_offset[R] > y_rows) return kCapacity;
-  for (int t = 0; t < T; ++t)
+  for (int t = 0; t < T; ++t) {
     for (int h = 0; h < H; ++h) {
       float acc = 0.0f;
       for (int r = 0; r < R; ++r) {
         int sl = L.slot[static_cast<size_t>(t) * R + r];
         if (sl < 0) continue;
         int64_t row = static_cast<int64_t>(L.rank_offset[r]) + sl;
-        acc = acc + bf16_bits_to_float(y[row * H + h]);  // one RN add
+        acc = acc + combine_input(y_fp8, y, y_scales, H, row, h);  // one RN add
       }
       out[static_cast<size_t>(t) * H + h] = float_to_bf16_bits_rn(acc);
     }
+    if (!combined_topk_weights || !recv_topk_weights) continue;
+    for (int j = 0; j < k; ++j) {
+      float wsum = 0.0f;
+      for (int r = 0; r < R; ++r) {
+        int sl = L.slot[static_cast<size_t>(t) * R + r];
+        if (sl < 0) continue;
+        int64_t row = static_cast<int64_t>(L.rank_offset[r]) + sl;
+        wsum = wsum + recv_topk_weights[row * k + j];
+      }
+      combined_topk_weights[static_cast<size_t>(t) * k + j] = wsum;
+    }
+  }
   return kOk;
+}
+
+int ref_combine(int R, int E, int k, int T, int H, const int64_t* topk_idx, const uint16_t* y,
+                int64_t y_rows, uint16_t* out) {
+  return ref_combine_ex(R, E, k, T, H, topk_idx, 0, y, nullptr, y_rows, nullptr, out, nullptr);
 }
 
 int ref_ll_dispatch(int R, int E, int k, int T, int H, int M, int fp8, const uint16_t* x,
@@ -424,6 +490,95 @@ int ref_ll_combine(int R, int E, int k, int T, int H, int M, const int64_t* topk
         int64_t row = e * M + slot[static_cast<size_t>(t) * k + j];
         acc = std::fmaf(topk_weights[static_cast<size_t>(t) * k + j],
                         bf16_bits_to_float(y[row * H + h]), acc);
+      }
+      out[static_cast<size_t>(t) * H + h] = float_to_bf16_bits_rn(acc);
+    }
+  }
+  return kOk;
+}
+
+int ref_em_layout(int R, int E, int k, int T, const int64_t* topk_idx, int align, int* num_recv_per_expert,
+                  int* expert_offset, int* row_of) {
+  Shape s;
+  int st = check_shape(R, E, k, T, &s);
+  if (st != kOk) return st;
+  if (align < 1) return kInvalidArg;
+  if ((st = check_ids(s, topk_idx)) != kOk) return st;
+  std::vector<int> count, offset, row;
+  em_rows(s, topk_idx, align, &count, &offset, &row);
+  if (num_recv_per_expert) std::memcpy(num_recv_per_expert, count.data(), count.size() * sizeof(int));
+  if (expert_offset) std::memcpy(expert_offset, offset.data(), offset.size() * sizeof(int));
+  if (row_of) std::memcpy(row_of, row.data(), row.size() * sizeof(int));
+  return kOk;
+}
+
+int ref_em_dispatch(int R, int E, int k, int T, int H, int fp8, const uint16_t* x, const int64_t* topk_idx,
+                    const float* topk_weights, int align, int64_t capacity_rows, void* recv_x,
+                    float* recv_scales, int64_t scales_ld, int* recv_src_idx, float* recv_weights) {
+  Shape s;
+  int st = check_shape(R, E, k, T, &s);
+  if (st != kOk) return st;
+  if (H <= 0 || H % 128 != 0 || align < 1 || capacity_rows < 0) return kInvalidArg;
+  if (fp8 && (!recv_scales || scales_ld < capacity_rows)) return kInvalidArg;
+  if ((st = check_ids(s, topk_idx)) != kOk) return st;
+  std::vector<int> count, offset, row;
+  em_rows(s, topk_idx, align, &count, &offset, &row);
+  const int G = H / 128;
+  // padding rows (and every row before the entries land): no source, weight 0
+  const int64_t used = offset[E] < capacity_rows ? offset[E] : capacity_rows;
+  for (int64_t i = 0; i < used; ++i) {
+    if (recv_src_idx) recv_src_idx[i] = -1;
+    if (recv_weights) recv_weights[i] = 0.0f;
+  }
+  std::vector<uint8_t> q(H);
+  std::vector<float> sc(G);
+  bool overflow = false;
+  for (int t = 0; t < T; ++t) {
+    const uint16_t* xt = x + static_cast<size_t>(t) * H;
+    if (fp8) quantize_row(H, xt, q.data(), sc.data());
+    for (int j = 0; j < k; ++j) {
+      int64_t rw = row[static_cast<size_t>(t) * k + j];
+      if (rw < 0) continue;
+      if (rw >= capacity_rows) { overflow = true; continue; }
+      if (fp8) {
+        std::memcpy(static_cast<uint8_t*>(recv_x) + rw * H, q.data(), H);
+        for (int g = 0; g < G; ++g) recv_scales[g * scales_ld + rw] = sc[g];
+      } else {
+        std::memcpy(static_cast<uint16_t*>(recv_x) + rw * H, xt, H * sizeof(uint16_t));
+      }
+      if (recv_src_idx) recv_src_idx[rw] = t;
+      if (recv_weights && topk_weights) recv_weights[rw] = topk_weights[static_cast<size_t>(t) * k + j];
+    }
+  }
+  return overflow ? kCapacity : kOk;
+}
+
+int ref_em_combine(int R, int E, int k, int T, int H, const int64_t* topk_idx, int align, const uint16_t* y,
+                   int64_t y_rows, uint16_t* out) {
+  Shape s;
+  int st = check_shape(R, E, k, T, &s);
+  if (st != kOk) return st;
+  if (H <= 0 || H % 128 != 0 || align < 1) return kInvalidArg;
+  if ((st = check_ids(s, topk_idx)) != kOk) return st;
+  std::vector<int> count, offset, row;
+  em_rows(s, topk_idx, align, &count, &offset, &row);
+  if (offset[E] > y_rows) return kCapacity;
+  std::vector<int> by_expert(k);
+  for (int t = 0; t < T; ++t) {
+    const int64_t* ids = topk_idx + static_cast<size_t>(t) * k;
+    // unmasked k-indices sorted by expert id, stable (insertion sort)
+    int n = 0;
+    for (int j = 0; j < k; ++j) {
+      if (ids[j] < 0) continue;
+      int at = n++;
+      for (; at > 0 && ids[by_expert[at - 1]] > ids[j]; --at) by_expert[at] = by_expert[at - 1];
+      by_expert[at] = j;
+    }
+    for (int h = 0; h < H; ++h) {
+      float acc = 0.0f;
+      for (int i = 0; i < n; ++i) {
+        int64_t rw = row[static_cast<size_t>(t) * k + by_expert[i]];
+        acc = acc + bf16_bits_to_float(y[rw * H + h]);  // one RN add
       }
       out[static_cast<size_t>(t) * H + h] = float_to_bf16_bits_rn(acc);
     }

@@ -52,6 +52,16 @@ int ref_dispatch(int R, int E, int k, int T, int H, int fp8, const uint16_t* x,
 int ref_combine(int R, int E, int k, int T, int H, const int64_t* topk_idx, const uint16_t* y,
                 int64_t y_rows, uint16_t* out);
 
+/* normal combine, general form: y is bf16 (y_fp8 = 0) or e4m3 bytes with
+ * fp32 scales y_scales [y_rows][H/128] (y_fp8 = 1), dequantised as
+ * decode(q) * scale.  If recv_topk_weights [y_rows][k] and
+ * combined_topk_weights [T][k] are both given, the per-row weights are also
+ * summed back to the source token, column by column, in ascending rank
+ * order.  ref_combine is this with bf16 y and no weights. */
+int ref_combine_ex(int R, int E, int k, int T, int H, const int64_t* topk_idx, int y_fp8, const void* y,
+                   const float* y_scales, int64_t y_rows, const float* recv_topk_weights, uint16_t* out,
+                   float* combined_topk_weights);
+
 /* low-latency dispatch into the expert-major buffer [E][M][H] (expert
  * e = rank e / E_l, local expert e % E_l): recv_scales [E][M][H/128] (fp8),
  * recv_src_info [E][M] (source token), recv_count [E], slot_out [T][k]
@@ -64,6 +74,28 @@ int ref_ll_dispatch(int R, int E, int k, int T, int H, int M, int fp8, const uin
 /* low-latency combine: out [T][H] bf16 = weighted sum of y [E][M][H] bf16. */
 int ref_ll_combine(int R, int E, int k, int T, int H, int M, const int64_t* topk_idx,
                    const float* topk_weights, const uint16_t* y, uint16_t* out);
+
+/* expert-major ("GEMM") layout: num_recv_per_expert [E], expert_offset
+ * [E+1] (first row of each expert's group; groups padded to multiples of
+ * align rows), row_of [T][k] (row of each entry, -1 if masked).  Any output
+ * may be NULL. */
+int ref_em_layout(int R, int E, int k, int T, const int64_t* topk_idx, int align, int* num_recv_per_expert,
+                  int* expert_offset, int* row_of);
+
+/* expert-major dispatch: recv_x [capacity_rows][H] (e4m3 or bf16),
+ * recv_scales [H/128][scales_ld] group-major (fp8 only, scales_ld >=
+ * capacity_rows), recv_src_idx [rows] (source token, -1 on padding rows),
+ * recv_weights [rows] (the entry's top-k weight, 0 on padding rows).
+ * Padding rows' recv_x / recv_scales are not written.  topk_weights,
+ * recv_src_idx, recv_weights may be NULL. */
+int ref_em_dispatch(int R, int E, int k, int T, int H, int fp8, const uint16_t* x, const int64_t* topk_idx,
+                    const float* topk_weights, int align, int64_t capacity_rows, void* recv_x,
+                    float* recv_scales, int64_t scales_ld, int* recv_src_idx, float* recv_weights);
+
+/* expert-major combine: out [T][H] bf16 = unweighted sum of the token's rows
+ * of y [y_rows][H] bf16 in ascending expert id. */
+int ref_em_combine(int R, int E, int k, int T, int H, const int64_t* topk_idx, int align, const uint16_t* y,
+                   int64_t y_rows, uint16_t* out);
 
 #ifdef __cplusplus
 }

@@ -13,6 +13,7 @@ import pytest
 
 import oracle
 import test_oracle_formats as fmt
+import test_oracle_em_combine as em
 import test_oracle_routing as rt
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "ep_oracle.cpp")
@@ -36,6 +37,25 @@ MUTANTS = {
     "ll_combine_k_order": ("while (pos > 0 && topk_idx[static_cast<size_t>(t) * k + order[pos - 1]] > e)", "while (false)"),
     # bf16 rounding truncates
     "bf16_truncates": ("if (dropped > 0x8000u || (dropped == 0x8000u && (keep & 1u))) keep += 1u;", ""),
+    # e4m3 combine input used without its scale
+    "fp8_combine_ignores_scale": ("return code_value * y_scales[row * (H / 128) + h / 128];", "return code_value;"),
+    # e4m3 combine input scaled by the row's first group only
+    "fp8_combine_first_group_scale": ("y_scales[row * (H / 128) + h / 128]", "y_scales[row * (H / 128)]"),
+    # top-k weights summed in descending rank order
+    "combined_weights_descending": ("for (int r = 0; r < R; ++r) {\n        int sl = L.slot[static_cast<size_t>(t) * R + r];\n        if (sl < 0) continue;\n        int64_t row = static_cast<int64_t>(L.rank_offset[r]) + sl;\n        wsum",
+                                    "for (int r = R - 1; r >= 0; --r) {\n        int sl = L.slot[static_cast<size_t>(t) * R + r];\n        if (sl < 0) continue;\n        int64_t row = static_cast<int64_t>(L.rank_offset[r]) + sl;\n        wsum"),
+    # expert groups not padded to the alignment
+    "em_groups_unaligned": ("int padded = ((*count)[e] + align - 1) / align * align;", "int padded = (*count)[e];"),
+    # expert-major rows handed out in (k-index, token) order
+    "em_rows_k_major": ("for (int t = 0; t < s.T; ++t)\n    for (int j = 0; j < s.k; ++j) {\n      int64_t e = topk_idx[static_cast<size_t>(t) * s.k + j];\n      if (e < 0) continue;\n      rank_in_expert",
+                        "for (int j = 0; j < s.k; ++j)\n    for (int t = 0; t < s.T; ++t) {\n      int64_t e = topk_idx[static_cast<size_t>(t) * s.k + j];\n      if (e < 0) continue;\n      rank_in_expert"),
+    # expert-major scales stored row-major
+    "em_scales_row_major": ("recv_scales[g * scales_ld + rw] = sc[g];", "recv_scales[rw * G + g] = sc[g];"),
+    # expert-major row weight taken from the token's first entry
+    "em_weight_first_entry": ("recv_weights[rw] = topk_weights[static_cast<size_t>(t) * k + j];",
+                              "recv_weights[rw] = topk_weights[static_cast<size_t>(t) * k];"),
+    # expert-major combine in k-index order
+    "em_combine_k_order": ("for (; at > 0 && ids[by_expert[at - 1]] > ids[j]; --at)", "for (; false; --at)"),
     # local expert id off by one rank
     "local_id_wrong_rank": ("here ? static_cast<int>(e - r * s.El) : -1", "here ? static_cast<int>(e - (r > 0 ? r - 1 : 0) * s.El) : -1"),
 }
@@ -58,6 +78,15 @@ def _pins(golden_dir):
         ("combine closed form", lambda: rt.test_combine_identity_expert_closed_form(8, 64, 8)),
         ("ll brute force", lambda: rt.test_ll_slots_and_counts_vs_sort(0.3)),
         ("ll exact", rt.test_ll_combine_brute_force_exact),
+        ("combine weights order hand", lambda: em.test_combine_weights_order_hand_worked(golden_dir)),
+        ("combine weights undo dispatch", lambda: em.test_combine_weights_undo_dispatch(8, 64, 8, 0.2)),
+        ("fp8 combine closed form", lambda: em.test_fp8_combine_power_of_two_scales_closed_form(8, 64, 8)),
+        ("fp8 combine bound", em.test_fp8_combine_general_within_bound),
+        ("em hand", lambda: em.test_em_layout_hand_worked(golden_dir)),
+        ("em brute force", lambda: em.test_em_layout_vs_sorted_entries(96, 8, 64, 6, 0.05, 0.1, 4)),
+        ("em rows", lambda: em.test_em_dispatch_rows_and_padding(True)),
+        ("em combine order hand", lambda: em.test_em_combine_order_hand_worked(golden_dir)),
+        ("em combine closed form", lambda: em.test_em_combine_identity_expert_closed_form(8, 64, 8, 16)),
     ]
     return calls
 
