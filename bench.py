@@ -3,7 +3,7 @@
 One step = one pass of the whole hot path over one batch of the
 DeepSeek-V3-shaped EP8 workload (8192 tokens, hidden 7168, 256 experts,
 top-8, 8 logical ranks):
-    layout -> FP8 dispatch -> combine (forward)
+    layout + FP8 dispatch (one fused call) -> combine (forward)
     -> BF16 dispatch of grad_out -> combine of the expert grads (backward,
        reusing the handle)
     -> low-latency FP8 dispatch -> weighted low-latency combine.
@@ -38,17 +38,15 @@ from combine_ep_get_03_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "dispatch & combine logical GB/s and % of GB300 HBM roofline (V3 shape, 1 GPU)"
 UNIT = "GB/s"
-OPS = ["layout", "dispatch_fp8", "combine", "dispatch_bf16_bwd", "combine_bwd", "ll_dispatch_fp8", "ll_combine"]
-KERNEL_OF = {"layout": "k_layout", "dispatch_fp8": "k_scatter<fp8>", "combine": "k_combine<normal>",
+OPS = ["layout_dispatch_fp8", "combine", "dispatch_bf16_bwd", "combine_bwd", "ll_dispatch_fp8", "ll_combine"]
+KERNEL_OF = {"layout_dispatch_fp8": "k_route_scatter<fp8>", "combine": "k_combine<normal>",
              "dispatch_bf16_bwd": "k_scatter<bf16>", "combine_bwd": "k_combine<normal>",
-             "ll_dispatch_fp8": "k_ll_route+k_scatter<fp8,ll>", "ll_combine": "k_combine<ll>"}
+             "ll_dispatch_fp8": "k_route_scatter<fp8,ll>", "ll_combine": "k_combine<ll>"}
 KERNEL_SOURCES = {"k_combine<normal>": ["combine.cu", "device_common.cuh"],
                   "k_combine<ll>": ["combine.cu", "device_common.cuh"],
-                  "k_scatter<fp8>": ["scatter_tma.cu", "device_common.cuh"],
-                  "k_scatter<bf16>": ["scatter_tma.cu", "device_common.cuh"],
-                  "k_ll_route+k_scatter<fp8,ll>": ["ll_dispatch.cu", "routing.cuh", "scatter_tma.cu",
-                                                   "device_common.cuh"],
-                  "k_layout": ["layout.cu", "routing.cuh", "device_common.cuh"]}
+                  "k_route_scatter<fp8>": ["dispatch_fused.cu", "scatter_common.cuh", "device_common.cuh"],
+                  "k_route_scatter<fp8,ll>": ["dispatch_fused.cu", "scatter_common.cuh", "device_common.cuh"],
+                  "k_scatter<bf16>": ["scatter_tma.cu", "scatter_common.cuh", "device_common.cuh"]}
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
 # ncu capture of the V3-shaped workload, keyed by the kernel's source digest:
 # a kernel whose sources changed since its capture reports traffic = null.
@@ -86,8 +84,7 @@ class Sizes:
         row8 = H + 4 * G        # e4m3 row + its fp32 scales
         row16 = 2 * H           # bf16 row
         self.logical = {
-            "layout": 0,
-            "dispatch_fp8": P * row8,
+            "layout_dispatch_fp8": P * row8,
             "combine": P * row16,
             "dispatch_bf16_bwd": P * row16,
             "combine_bwd": P * row16,
@@ -96,8 +93,9 @@ class Sizes:
         }
         dst = 8 * T * kmax      # the handle's (rank, row) list per token
         self.hbm = {
-            "layout": 8 * T * k + 4 * T * k + dst,
-            "dispatch_fp8": 2 * T * H + P * row8 + P * (4 + 8 * k) + dst + 8 * T * k,
+            # layout (ids in; int32 ids and the (rank, row) list out) + FP8 dispatch
+            "layout_dispatch_fp8": (8 * T * k + 4 * T * k + dst) + (2 * T * H + P * row8 + P * (4 + 8 * k) + dst
+                                                                    + 8 * T * k),
             "combine": P * row16 + 2 * T * H + dst,
             "dispatch_bf16_bwd": 2 * T * H + P * row16 + dst,
             "combine_bwd": P * row16 + 2 * T * H + dst,
@@ -163,10 +161,9 @@ class Step:
     def ops(self):
         h, n = self.h, self.num_sms
         return [
-            ("layout", lambda: h.get_dispatch_layout(self.idx)),
-            ("dispatch_fp8", lambda: h.dispatch(self.x, self.wts, ep.EP_FP8_E4M3, self.recv, self.scales,
-                                                recv_src_idx=self.src, recv_topk_idx=self.ridx,
-                                                recv_topk_weights=self.rw, num_sms=n)),
+            ("layout_dispatch_fp8", lambda: h.layout_and_dispatch(
+                self.idx, self.x, self.wts, ep.EP_FP8_E4M3, self.recv, self.scales, recv_src_idx=self.src,
+                recv_topk_idx=self.ridx, recv_topk_weights=self.rw, num_sms=n)),
             ("combine", lambda: h.combine(self.y, self.out, num_sms=n)),
             ("dispatch_bf16_bwd", lambda: h.dispatch(self.grad_out, None, ep.EP_BF16, self.grad_in, num_sms=n)),
             ("combine_bwd", lambda: h.combine(self.grad_recv, self.grad_x, num_sms=n)),
@@ -288,7 +285,7 @@ def e2e_steps(step: Step, K: int, stream: torch.cuda.Stream):
     for _ in range(K):
         for name in ("x", "idx", "wts", "y", "grad_out", "grad_recv"):
             getattr(step, name).copy_(pin[name], non_blocking=True)
-        for name in ("layout", "dispatch_fp8", "combine", "dispatch_bf16_bwd", "combine_bwd", "ll_dispatch_fp8"):
+        for name in ("layout_dispatch_fp8", "combine", "dispatch_bf16_bwd", "combine_bwd", "ll_dispatch_fp8"):
             ops[name]()
         counts.copy_(step.ll_cnt, non_blocking=True)
         stream.synchronize()

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libep_gb300.so")
-SOURCES = ["api.cu", "layout.cu", "dispatch.cu", "combine.cu", "ll_dispatch.cu", "layout_noalloc.cu", "scatter_tma.cu"]
+SOURCES = ["api.cu", "layout.cu", "dispatch.cu", "combine.cu", "ll_dispatch.cu", "layout_noalloc.cu", "scatter_tma.cu", "dispatch_fused.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

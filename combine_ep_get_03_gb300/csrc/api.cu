@@ -13,13 +13,14 @@
 struct ep_handle {
   int R, E, k, H, max_tpr, El, kmax, kp_log2;
   int Tmax;
+  int ids32;  // top-k ids are int32 (else int64)
   int device, num_sms;
   // routing configuration
   int layout_CT, ll_CT;
   size_t layout_smem, ll_smem, layout_tokens_smem;
   int layout_cmax, ll_cmax;
   // occupancy (blocks per SM) of the persistent kernels
-  int occ_dispatch[2], occ_combine[2];
+  int occ_dispatch[2], occ_combine[4];  // combine: rank-major bf16, rank-major e4m3, low latency, expert-major
   // TMA scatter: row stages and consumer warps per block for
   // [fp8][low_latency]; 0 stages = rows too long, the register-resident
   // kernels are used instead
@@ -41,6 +42,9 @@ struct ep_handle {
   unsigned long long* layout_flags;
   unsigned long long* ll_flags;
   unsigned long long* tickets;  // [0] layout, [1] low latency: (epoch << 32) | next chunk id
+  int* fused_agg;               // [num_sms][R+E] per-block counts of the fused kernel
+  unsigned* fused_barrier;      // [2] its grid barrier words
+  size_t smem_optin;
   int* err;
   // pinned host mirror: err, then R + E + R+1 counts
   int* host;
@@ -62,6 +66,19 @@ bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+bool ids_aligned(const ep_handle* h, const void* topk_idx) {
+  return !topk_idx || (h->ids32 ? aligned4(topk_idx) : aligned8(topk_idx));
+}
+
+// EP_NUM_TOPK_IDX_BITS: 64 (default) or 32; anything else is an error (-1).
+int ids32_from_env() {
+  const char* v = std::getenv("EP_NUM_TOPK_IDX_BITS");
+  if (!v || !*v) return 0;
+  if (std::strcmp(v, "64") == 0) return 0;
+  if (std::strcmp(v, "32") == 0) return 1;
+  return -1;
+}
+
 ep_status_t check_device(const ep_handle* h) {
   int d = -1;
   if (cudaGetDevice(&d) != cudaSuccess) return EP_ERR_CUDA;
@@ -76,10 +93,11 @@ int grid_for(const ep_handle* h, int occ, int num_sms, int T, int warps_per_bloc
   return blocks > 0 ? blocks : 1;
 }
 
-RouteParams route_params(ep_handle* h, const int64_t* topk_idx, int T, int CT,
+RouteParams route_params(ep_handle* h, const void* topk_idx, int T, int CT,
                          unsigned long long* flags, unsigned long long* ticket) {
   RouteParams p;
   p.topk_idx = topk_idx;
+  p.ids32 = h->ids32;
   p.T = T;
   p.R = h->R;
   p.E = h->E;
@@ -95,6 +113,29 @@ RouteParams route_params(ep_handle* h, const int64_t* topk_idx, int T, int CT,
   p.ticket = ticket;
   p.err = h->err;
   return p;
+}
+
+int sms_for(const ep_handle* h, int num_sms) {
+  return num_sms <= 0 ? h->num_sms : (num_sms < h->num_sms ? num_sms : h->num_sms);
+}
+
+ep::FusedArgs fused_args(ep_handle* h, const void* topk_idx, const uint16_t* x, const float* w, int T) {
+  ep::FusedArgs f{};
+  f.topk_idx = topk_idx;
+  f.ids32 = h->ids32;
+  f.x = x;
+  f.topk_weights = w;
+  f.T = T;
+  f.R = h->R;
+  f.E = h->E;
+  f.El = h->El;
+  f.k = h->k;
+  f.kp_log2 = h->kp_log2;
+  f.kmax = h->kmax;
+  f.H = h->H;
+  f.barrier = h->fused_barrier;
+  f.err = h->err;
+  return f;
 }
 
 }  // namespace
@@ -135,6 +176,11 @@ ep_status_t ep_handle_create(int R, int E, int k, int H, int max_tpr, ep_handle_
   while (kp < k) kp <<= 1, ++lg;
   h->kp_log2 = lg;
   h->Tmax = R * max_tpr;
+  h->ids32 = ids32_from_env();
+  if (h->ids32 < 0) {
+    delete h;
+    return EP_ERR_INVALID_ARG;
+  }
   h->T_layout = -1;
   h->T_ll = -1;
   h->debug = std::getenv("EP_DEBUG") != nullptr;
@@ -185,6 +231,8 @@ ep_status_t ep_handle_create(int R, int E, int k, int H, int max_tpr, ep_handle_
   const size_t o_lf = take(sizeof(unsigned long long) * static_cast<size_t>(h->layout_cmax) * NKl);
   const size_t o_llf = take(sizeof(unsigned long long) * static_cast<size_t>(h->ll_cmax) * NKll);
   const size_t o_tk = take(sizeof(unsigned long long) * 2);
+  const size_t o_fagg = take(sizeof(int) * static_cast<size_t>(h->num_sms) * (R + E));
+  const size_t o_fbar = take(sizeof(unsigned) * 2);
   const size_t o_err = take(sizeof(int));
   if ((st = cuda_status(cudaMalloc(&h->arena, off), "cudaMalloc")) != EP_OK) {
     delete h;
@@ -201,6 +249,8 @@ ep_status_t ep_handle_create(int R, int E, int k, int H, int max_tpr, ep_handle_
   h->layout_flags = reinterpret_cast<unsigned long long*>(base + o_lf);
   h->ll_flags = reinterpret_cast<unsigned long long*>(base + o_llf);
   h->tickets = reinterpret_cast<unsigned long long*>(base + o_tk);
+  h->fused_agg = reinterpret_cast<int*>(base + o_fagg);
+  h->fused_barrier = reinterpret_cast<unsigned*>(base + o_fbar);
   h->err = reinterpret_cast<int*>(base + o_err);
   // zero everything once (latch, look-back words); tickets start at epoch 1,
   // so no look-back word ever matches before it is written
@@ -217,6 +267,7 @@ ep_status_t ep_handle_create(int R, int E, int k, int H, int max_tpr, ep_handle_
   // in the space sized for the fused kernel's smaller chunks)
   h->ll_route_smem = ep::route_smem_bytes(NKll, h->layout_CT << lg, h->layout_CT, h->kmax);
   const size_t optin = static_cast<size_t>(prop.sharedMemPerBlockOptin);
+  h->smem_optin = optin;
   for (int f = 0; f < 2; ++f)
     for (int l = 0; l < 2; ++l) ep::scatter_config(H, R, f == 1, l == 1, optin, &h->scatter_ns[f][l], &h->scatter_nc[f][l]);
   if ((st = cuda_status(ep::configure_layout(h->layout_smem), "configure_layout")) != EP_OK ||
@@ -224,7 +275,8 @@ ep_status_t ep_handle_create(int R, int E, int k, int H, int max_tpr, ep_handle_
       (st = cuda_status(ep::configure_ll_route(h->ll_route_smem), "configure_ll_route")) != EP_OK ||
       (R <= 64 &&
        (st = cuda_status(ep::configure_layout_tokens(h->layout_tokens_smem), "configure_layout_tokens")) != EP_OK) ||
-      (st = cuda_status(ep::configure_scatter(optin), "configure_scatter")) != EP_OK) {
+      (st = cuda_status(ep::configure_scatter(optin), "configure_scatter")) != EP_OK ||
+      (st = cuda_status(ep::configure_fused(optin), "configure_fused")) != EP_OK) {
     ep_handle_destroy(h);
     return st;
   }
@@ -232,7 +284,12 @@ ep_status_t ep_handle_create(int R, int E, int k, int H, int max_tpr, ep_handle_
     int occ = 0;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, ep::dispatch_kernel(m == 1), ep::dispatch_threads(), 0);
     h->occ_dispatch[m] = occ > 0 ? occ : 1;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, ep::combine_kernel(m == 1), ep::combine_threads(), 0);
+  }
+  for (int m = 0; m < 4; ++m) {
+    const int src = m < 2 ? ep::kSrcRanks : m == 2 ? ep::kSrcLowLatency : ep::kSrcExpertMajor;
+    int occ = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, ep::combine_kernel(src, m == 1), ep::combine_threads(),
+                                                  ep::combine_smem_bytes(src, R, E));
     h->occ_combine[m] = occ > 0 ? occ : 1;
   }
   if (h->debug)
@@ -256,11 +313,11 @@ ep_status_t ep_handle_destroy(ep_handle_t h) {
   return EP_OK;
 }
 
-ep_status_t ep_get_dispatch_layout(ep_handle_t h, const int64_t* topk_idx, int T, int* num_tokens_per_rank,
+ep_status_t ep_get_dispatch_layout(ep_handle_t h, const void* topk_idx, int T, int* num_tokens_per_rank,
                                    int* num_tokens_per_expert, uint8_t* is_token_in_rank, ep_stream_t stream) {
   if (!h) return EP_ERR_INVALID_ARG;
   if (T < 0 || T % h->R != 0 || T > h->Tmax || (T > 0 && !topk_idx)) return EP_ERR_INVALID_ARG;
-  if ((topk_idx && !aligned8(topk_idx)) || (num_tokens_per_rank && !aligned4(num_tokens_per_rank)) ||
+  if (!ids_aligned(h, topk_idx) || (num_tokens_per_rank && !aligned4(num_tokens_per_rank)) ||
       (num_tokens_per_expert && !aligned4(num_tokens_per_expert)))
     return EP_ERR_INVALID_ARG;
   ep_status_t st = check_device(h);
@@ -388,17 +445,76 @@ ep_status_t ep_dispatch(ep_handle_t h, const void* x, const float* topk_weights,
   return cuda_status(cudaGetLastError(), "k_dispatch launch");
 }
 
-ep_status_t ep_combine(ep_handle_t h, const void* y, int64_t y_rows, void* out, int num_sms, ep_stream_t stream) {
+ep_status_t ep_layout_and_dispatch(ep_handle_t h, const void* topk_idx, int T, const void* x,
+                                   const float* topk_weights, ep_dtype_t dtype, void* recv_x, float* recv_scales,
+                                   int64_t cap, int* recv_src_idx, int* recv_topk_idx, float* recv_topk_weights,
+                                   int num_sms, ep_stream_t stream) {
+  if (!h) return EP_ERR_INVALID_ARG;
+  if (dtype != EP_BF16 && dtype != EP_FP8_E4M3) return EP_ERR_INVALID_ARG;
+  const bool fp8 = dtype == EP_FP8_E4M3;
+  if (T < 0 || T % h->R != 0 || T > h->Tmax || (T > 0 && (!topk_idx || !x)) || cap < 0 ||
+      (cap > 0 && !recv_x) || (fp8 && cap > 0 && !recv_scales))
+    return EP_ERR_INVALID_ARG;
+  if (recv_topk_weights && !topk_weights) return EP_ERR_INVALID_ARG;
+  if (!ids_aligned(h, topk_idx) || (x && !aligned16(x)) || (recv_x && !aligned16(recv_x)) ||
+      (fp8 && recv_scales && !aligned4(recv_scales)) || (topk_weights && !aligned4(topk_weights)) ||
+      (recv_src_idx && !aligned4(recv_src_idx)) || (recv_topk_idx && !aligned4(recv_topk_idx)) ||
+      (recv_topk_weights && !aligned4(recv_topk_weights)))
+    return EP_ERR_INVALID_ARG;
+  ep_status_t st = check_device(h);
+  if (st != EP_OK) return st;
+  int fblocks = 0, fns = 0, fnc = 0;
+  if (static_cast<long long>(T) * h->kmax < (1LL << 31))
+    ep::fused_config(false, fp8, T, h->R, h->E, h->k, h->kmax, h->H, sms_for(h, num_sms), h->smem_optin, &fblocks,
+                     &fns, &fnc);
+  if (fblocks == 0) {
+    // the general path: layout kernel, then the scatter
+    if ((st = ep_get_dispatch_layout(h, topk_idx, T, nullptr, nullptr, nullptr, stream)) != EP_OK) return st;
+    return ep_dispatch(h, x, topk_weights, dtype, recv_x, recv_scales, cap, recv_src_idx, recv_topk_idx,
+                       recv_topk_weights, num_sms, stream);
+  }
+  ep::FusedArgs f = fused_args(h, topk_idx, static_cast<const uint16_t*>(x), topk_weights, T);
+  f.agg = h->fused_agg;
+  f.dst = h->dst;
+  f.idx32 = h->idx32;
+  f.recv_per_rank = h->recv_per_rank;
+  f.rank_offset = h->rank_offset;
+  f.recv_per_expert = h->recv_per_expert;
+  f.cap = cap;
+  f.recv_src_idx = recv_src_idx;
+  f.recv_topk_idx = recv_topk_idx;
+  f.recv_topk_weights = recv_topk_weights;
+  f.recv_x = recv_x;
+  f.recv_scales = recv_scales;
+  if ((st = cuda_status(ep::launch_fused(f, fp8, false, fblocks, fns, fnc, reinterpret_cast<cudaStream_t>(stream)),
+                        "k_route_scatter launch")) != EP_OK)
+    return st;
+  if (h->debug)
+    std::fprintf(stderr, "[ep] layout+dispatch %s T=%d: fused, %d blocks, %d stages, %d consumers\n",
+                 fp8 ? "fp8" : "bf16", T, fblocks, fns, fnc);
+  h->T_layout = T;
+  return EP_OK;
+}
+
+ep_status_t ep_combine_ex(ep_handle_t h, ep_dtype_t y_dtype, const void* y, const float* y_scales, int64_t y_rows,
+                          const float* recv_topk_weights, void* out, float* combined_topk_weights, int num_sms,
+                          ep_stream_t stream) {
   if (!h) return EP_ERR_INVALID_ARG;
   if (h->T_layout < 0) return EP_ERR_STATE;
+  if (y_dtype != EP_BF16 && y_dtype != EP_FP8_E4M3) return EP_ERR_INVALID_ARG;
+  const bool fp8 = y_dtype == EP_FP8_E4M3;
   const int T = h->T_layout;
-  if (y_rows < 0 || (T > 0 && (!out || (y_rows > 0 && !y)))) return EP_ERR_INVALID_ARG;
-  if ((y && !aligned16(y)) || (out && !aligned16(out))) return EP_ERR_INVALID_ARG;
+  if (y_rows < 0 || (T > 0 && (!out || (y_rows > 0 && (!y || (fp8 && !y_scales)))))) return EP_ERR_INVALID_ARG;
+  if ((recv_topk_weights != nullptr) != (combined_topk_weights != nullptr)) return EP_ERR_INVALID_ARG;
+  if ((y && !aligned16(y)) || (out && !aligned16(out)) || (fp8 && y_scales && !aligned4(y_scales)) ||
+      (recv_topk_weights && !aligned4(recv_topk_weights)) || (combined_topk_weights && !aligned4(combined_topk_weights)))
+    return EP_ERR_INVALID_ARG;
   ep_status_t st = check_device(h);
   if (st != EP_OK) return st;
   if (T == 0) return EP_OK;
   ep::CombineArgs a{};
-  a.y = static_cast<const uint16_t*>(y);
+  a.y = y;
+  a.y_scales = fp8 ? y_scales : nullptr;
   a.out = static_cast<uint16_t*>(out);
   a.y_rows = y_rows;
   a.T = T;
@@ -406,16 +522,24 @@ ep_status_t ep_combine(ep_handle_t h, const void* y, int64_t y_rows, void* out, 
   a.k = h->k;
   a.kmax = h->kmax;
   a.R = h->R;
+  a.E = h->E;
   a.dst = h->dst;
   a.rank_offset = h->rank_offset;
+  a.recv_topk_weights = recv_topk_weights;
+  a.combined_topk_weights = combined_topk_weights;
   a.err = h->err;
-  const int blocks = grid_for(h, h->occ_combine[0], num_sms, T * ((h->H + 1023) / 1024), ep::combine_threads() / 32);
-  ep::launch_combine(a, false, blocks, reinterpret_cast<cudaStream_t>(stream));
-  if (h->debug) std::fprintf(stderr, "[ep] combine T=%d: %d blocks\n", T, blocks);
+  const int blocks =
+      grid_for(h, h->occ_combine[fp8 ? 1 : 0], num_sms, T * ((h->H + 1023) / 1024), ep::combine_threads() / 32);
+  ep::launch_combine(a, ep::kSrcRanks, fp8, blocks, reinterpret_cast<cudaStream_t>(stream));
+  if (h->debug) std::fprintf(stderr, "[ep] combine %s T=%d: %d blocks\n", fp8 ? "e4m3" : "bf16", T, blocks);
   return cuda_status(cudaGetLastError(), "k_combine launch");
 }
 
-ep_status_t ep_low_latency_dispatch(ep_handle_t h, const void* x, const int64_t* topk_idx, int T, ep_dtype_t dtype,
+ep_status_t ep_combine(ep_handle_t h, const void* y, int64_t y_rows, void* out, int num_sms, ep_stream_t stream) {
+  return ep_combine_ex(h, EP_BF16, y, nullptr, y_rows, nullptr, out, nullptr, num_sms, stream);
+}
+
+ep_status_t ep_low_latency_dispatch(ep_handle_t h, const void* x, const void* topk_idx, int T, ep_dtype_t dtype,
                                     void* recv_x, float* recv_scales, int* recv_src_info, int* recv_count,
                                     int num_sms, ep_stream_t stream) {
   if (!h) return EP_ERR_INVALID_ARG;
@@ -423,7 +547,7 @@ ep_status_t ep_low_latency_dispatch(ep_handle_t h, const void* x, const int64_t*
   const bool fp8 = dtype == EP_FP8_E4M3;
   if (T < 0 || T % h->R != 0 || T > h->Tmax) return EP_ERR_INVALID_ARG;
   if (T > 0 && (!x || !topk_idx || !recv_x || (fp8 && !recv_scales))) return EP_ERR_INVALID_ARG;
-  if ((x && !aligned16(x)) || (topk_idx && !aligned8(topk_idx)) || (recv_x && !aligned16(recv_x)) ||
+  if ((x && !aligned16(x)) || !ids_aligned(h, topk_idx) || (recv_x && !aligned16(recv_x)) ||
       (fp8 && recv_scales && !aligned4(recv_scales)) || (recv_src_info && !aligned4(recv_src_info)) ||
       (recv_count && !aligned4(recv_count)))
     return EP_ERR_INVALID_ARG;
@@ -434,6 +558,28 @@ ep_status_t ep_low_latency_dispatch(ep_handle_t h, const void* x, const int64_t*
   if (T == 0) {
     h->T_ll = 0;
     if (recv_count) return cuda_status(cudaMemsetAsync(recv_count, 0, sizeof(int) * h->E, s), "ll memset");
+    return EP_OK;
+  }
+  int fblocks = 0, fns = 0, fnc = 0;
+  ep::fused_config(true, fp8, T, h->R, h->E, h->k, h->kmax, h->H, sms_for(h, num_sms), h->smem_optin, &fblocks,
+                   &fns, &fnc);
+  if (fblocks > 0) {
+    // routing and row movement in one cooperative launch
+    ep::FusedArgs f = fused_args(h, topk_idx, static_cast<const uint16_t*>(x), nullptr, T);
+    f.M = M;
+    f.agg = h->fused_agg;
+    f.ll_idx = h->ll_idx;
+    f.ll_slot = h->ll_slot;
+    f.recv_count = recv_count;
+    f.recv_src_info = recv_src_info;
+    f.recv_x = recv_x;
+    f.recv_scales = recv_scales;
+    if ((st = cuda_status(ep::launch_fused(f, fp8, true, fblocks, fns, fnc, s), "k_route_scatter(ll) launch")) !=
+        EP_OK)
+      return st;
+    if (h->debug)
+      std::fprintf(stderr, "[ep] ll dispatch T=%d: fused, %d blocks, %d stages, %d consumers\n", T, fblocks, fns, fnc);
+    h->T_ll = T;
     return EP_OK;
   }
   const int sns = h->scatter_ns[fp8 ? 1 : 0][1], snc = h->scatter_nc[fp8 ? 1 : 0][1];
@@ -497,24 +643,33 @@ ep_status_t ep_low_latency_combine(ep_handle_t h, const void* y, const float* to
   if (st != EP_OK) return st;
   if (T == 0) return EP_OK;
   ep::CombineArgs a{};
-  a.y = static_cast<const uint16_t*>(y);
+  a.y = y;
   a.out = static_cast<uint16_t*>(out);
   a.y_rows = static_cast<long long>(h->E) * h->Tmax;
   a.T = T;
   a.H = h->H;
   a.k = h->k;
   a.kmax = h->kmax;
-  a.ll_idx = h->ll_idx;
-  a.ll_slot = h->ll_slot;
+  a.ent_idx = h->ll_idx;
+  a.ent_slot = h->ll_slot;
   a.topk_weights = topk_weights;
   a.M = h->Tmax;
   a.R = h->R;
+  a.E = h->E;
   a.err = h->err;
-  const int blocks = grid_for(h, h->occ_combine[1], num_sms, T * ((h->H + 1023) / 1024), ep::combine_threads() / 32);
-  ep::launch_combine(a, true, blocks, reinterpret_cast<cudaStream_t>(stream));
+  const int blocks = grid_for(h, h->occ_combine[2], num_sms, T * ((h->H + 1023) / 1024), ep::combine_threads() / 32);
+  ep::launch_combine(a, ep::kSrcLowLatency, false, blocks, reinterpret_cast<cudaStream_t>(stream));
   if (h->debug) std::fprintf(stderr, "[ep] ll combine T=%d: %d blocks\n", T, blocks);
   return cuda_status(cudaGetLastError(), "k_combine(ll) launch");
 }
+
+ep_status_t ep_handle_set_topk_idx_bits(ep_handle_t h, int bits) {
+  if (!h || (bits != 32 && bits != 64)) return EP_ERR_INVALID_ARG;
+  h->ids32 = bits == 32 ? 1 : 0;
+  return EP_OK;
+}
+
+int ep_handle_topk_idx_bits(ep_handle_t h) { return !h ? 0 : h->ids32 ? 32 : 64; }
 
 ep_status_t ep_get_device_status(ep_handle_t h, ep_stream_t stream) {
   if (!h) return EP_ERR_INVALID_ARG;

@@ -1,19 +1,27 @@
-// combine on sm_103a, both modes -- "DeepEP 要約" (stakiran.github.io)
+// combine on sm_103a, every receive layout -- "DeepEP 要約" (stakiran.github.io)
 // section 3: combine(y, handle) and low_latency_combine; the vi.news.hada.io
-// DeepEP article: combine reduces the expert outputs back to the
-// originating rank.
+// DeepEP article, "Mẫu sử dụng cho huấn luyện, prefill và decoding": combine
+// reduces the expert outputs back to the originating rank, and its backward
+// is a dispatch.
 //
-//  normal:       out[t] = bf16( sum over t's destination ranks, ascending,
-//                of fp32(y[row]) ), accumulated from +0.0 with RN adds;
+//  rank-major (normal):  out[t] = bf16( sum over t's destination ranks,
+//                ascending, of v(row) ), from +0.0 with RN adds, where v is
+//                the bf16 row widened, or an e4m3 row decoded and multiplied
+//                by its 128-channel group's scale (one RN multiply).
+//                Optionally also combined_w[t][j] = sum over the same rows,
+//                same order, of recv_w[row][j] (the top-k weights' reduction
+//                for the backward of the weights);
 //  low latency:  out[t] = bf16( acc ), acc = fmaf(w_j, fp32(y[row_j]), acc)
 //                over t's unmasked entries in ascending expert id (k-index
-//                breaks ties), from +0.0.
+//                breaks ties), from +0.0;
+//  expert-major: out[t] = bf16( sum of fp32(y[row_j]) ) over t's unmasked
+//                entries in ascending expert id, from +0.0 with RN adds.
 //
 // HBM-bound gather-reduce.  Work is split into (token, 1024-channel part)
 // items dealt round-robin to the warps of a persistent grid, so the last
-// round leaves few warps idle.  A warp takes a part 512 channels at a time
-// and requests every source row of the slab before summing any, so up to
-// kMaxSrc x 1 KB is in flight per warp.
+// round leaves few warps idle.  A warp takes a part one slab at a time (512
+// bf16 or 1024 e4m3 channels) and requests every source row of the slab
+// before summing any, so up to kMaxSrc x 1 KB is in flight per warp.
 #include <climits>
 
 #include "device_common.cuh"
@@ -23,20 +31,37 @@ namespace ep {
 
 constexpr int kCombineThreads = 256;
 constexpr int kCombineWarps = kCombineThreads / 32;
-constexpr int kChunks = 2;   // 16-byte chunks per lane per slab: slab = 32 * 2 * 8 = 512 channels
+constexpr int kChunks = 2;   // 16-byte chunks per lane per slab
 constexpr int kMaxSrc = 8;   // source rows loaded together
 constexpr int kPartChannels = 1024;  // channels of one work item
-constexpr int kMaxCachedRanks = 1024;
 
-template <bool kLL>
+// Two e4m3 codes (low byte first) -> two floats; exact (every e4m3 value is
+// an f16 value, and every f16 value an f32 value).
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes) {
+  float lo, hi;
+  asm("{\n\t.reg .b16 c, l, h;\n\t.reg .b32 p;\n\t"
+      "cvt.u16.u32 c, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 p, c;\n\t"
+      "mov.b32 {l, h}, p;\n\t"
+      "cvt.f32.f16 %0, l;\n\t"
+      "cvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(two_codes));
+  return make_float2(lo, hi);
+}
+
+template <int kSrc, bool kFP8>
 __global__ void __launch_bounds__(kCombineThreads) k_combine(CombineArgs a) {
-  __shared__ int so[kMaxCachedRanks + 1];  // rank_offset (normal mode)
+  extern __shared__ int base_smem[];  // rank_offset [R+1] or expert_offset [E+1]
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int nw = gridDim.x * kCombineWarps;
   const unsigned lt = lanemask_lt();
-  if (!kLL) {
-    for (int r = threadIdx.x; r <= a.R; r += kCombineThreads) so[r] = a.rank_offset[r];
+  if (kSrc == kSrcRanks) {
+    for (int r = threadIdx.x; r <= a.R; r += kCombineThreads) base_smem[r] = a.rank_offset[r];
+    __syncthreads();
+  } else if (kSrc == kSrcExpertMajor) {
+    for (int e = threadIdx.x; e <= a.E; e += kCombineThreads) base_smem[e] = a.expert_offset[e];
     __syncthreads();
   }
   const int parts = (a.H + kPartChannels - 1) / kPartChannels;
@@ -47,17 +72,17 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine(CombineArgs a) {
     long long row = -1;
     float w = 0.0f;
     int key = INT_MAX;
-    if (!kLL) {
+    if (kSrc == kSrcRanks) {
       if (lane < a.kmax) {
         const int2 d = a.dst[static_cast<size_t>(t) * a.kmax + lane];
-        if (d.x >= 0) row = static_cast<long long>(so[d.x]) + d.y;
+        if (d.x >= 0) row = static_cast<long long>(base_smem[d.x]) + d.y;
       }
     } else if (lane < a.k) {
-      const int e = a.ll_idx[static_cast<size_t>(t) * a.k + lane];
-      const int s = a.ll_slot[static_cast<size_t>(t) * a.k + lane];
+      const int e = a.ent_idx[static_cast<size_t>(t) * a.k + lane];
+      const int s = a.ent_slot[static_cast<size_t>(t) * a.k + lane];
       if (e >= 0 && s >= 0) {
-        row = static_cast<long long>(e) * a.M + s;
-        w = a.topk_weights[static_cast<size_t>(t) * a.k + lane];
+        row = kSrc == kSrcLowLatency ? static_cast<long long>(e) * a.M + s : static_cast<long long>(base_smem[e]) + s;
+        if (kSrc == kSrcLowLatency) w = a.topk_weights[static_cast<size_t>(t) * a.k + lane];
         key = e;
       }
     }
@@ -71,7 +96,7 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine(CombineArgs a) {
     const int n = __popc(vmask);
     // summation position of this lane's source
     int pos;
-    if (!kLL) {
+    if (kSrc == kSrcRanks) {
       pos = __popc(vmask & lt);  // the destination list is in ascending rank
     } else {
       pos = 0;
@@ -89,25 +114,43 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine(CombineArgs a) {
     const long long srow = __shfl_sync(kFullMask, row, from);
     const float sw = __shfl_sync(kFullMask, w, from);
 
-    const uint16_t* y = a.y;
+    if (kSrc == kSrcRanks && a.recv_topk_weights && part == 0) {
+      // the top-k weights, column `lane`, summed over the same rows in order
+      float ws = 0.0f;
+      for (int s = 0; s < n; ++s) {
+        const long long r_ = __shfl_sync(kFullMask, srow, s);
+        if (lane < a.k) ws = __fadd_rn(ws, a.recv_topk_weights[r_ * a.k + lane]);
+      }
+      if (lane < a.k) a.combined_topk_weights[static_cast<size_t>(t) * a.k + lane] = ws;
+    }
+
     uint16_t* out = a.out + static_cast<size_t>(t) * a.H;
     const int h_end = min(a.H, (part + 1) * kPartChannels);
-    for (int h0 = part * kPartChannels; h0 < h_end; h0 += 32 * kChunks * 8) {
-      float acc[kChunks][8];
+    constexpr int kLaneCh = kFP8 ? 16 : 8;  // channels per 16-byte chunk
+    for (int h0 = part * kPartChannels; h0 < h_end; h0 += 32 * kChunks * kLaneCh) {
+      float acc[kChunks][kLaneCh];
 #pragma unroll
       for (int c = 0; c < kChunks; ++c)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[c][i] = 0.0f;
+        for (int i = 0; i < kLaneCh; ++i) acc[c][i] = 0.0f;
       for (int sb = 0; sb < n; sb += kMaxSrc) {
         uint4 v[kMaxSrc][kChunks];
+        float sc[kMaxSrc][kChunks];
 #pragma unroll
         for (int s = 0; s < kMaxSrc; ++s) {
           const long long r_ = __shfl_sync(kFullMask, srow, (sb + s) & 31);
           if (sb + s < n) {
 #pragma unroll
             for (int c = 0; c < kChunks; ++c) {
-              const int ch = h0 + (c * 32 + lane) * 8;
-              v[s][c] = ch < h_end ? ld_stream(y + r_ * a.H + ch) : make_uint4(0, 0, 0, 0);
+              const int ch = h0 + (c * 32 + lane) * kLaneCh;
+              if (kFP8) {
+                const uint8_t* yq = static_cast<const uint8_t*>(a.y);
+                v[s][c] = ch < h_end ? ld_stream(yq + r_ * a.H + ch) : make_uint4(0, 0, 0, 0);
+                sc[s][c] = ch < h_end ? __ldg(a.y_scales + r_ * (a.H >> 7) + (ch >> 7)) : 0.0f;
+              } else {
+                const uint16_t* yb = static_cast<const uint16_t*>(a.y);
+                v[s][c] = ch < h_end ? ld_stream(yb + r_ * a.H + ch) : make_uint4(0, 0, 0, 0);
+              }
             }
           }
         }
@@ -120,7 +163,14 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine(CombineArgs a) {
               const uint32_t q[4] = {v[s][c].x, v[s][c].y, v[s][c].z, v[s][c].w};
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
-                if (kLL) {
+                if (kFP8) {
+                  const float2 f01 = e4m3x2_to_float2(q[i] & 0xffffu);
+                  const float2 f23 = e4m3x2_to_float2(q[i] >> 16);
+                  acc[c][4 * i] = __fadd_rn(acc[c][4 * i], __fmul_rn(f01.x, sc[s][c]));
+                  acc[c][4 * i + 1] = __fadd_rn(acc[c][4 * i + 1], __fmul_rn(f01.y, sc[s][c]));
+                  acc[c][4 * i + 2] = __fadd_rn(acc[c][4 * i + 2], __fmul_rn(f23.x, sc[s][c]));
+                  acc[c][4 * i + 3] = __fadd_rn(acc[c][4 * i + 3], __fmul_rn(f23.y, sc[s][c]));
+                } else if (kSrc == kSrcLowLatency) {
                   acc[c][2 * i] = __fmaf_rn(ws, bf16_lo(q[i]), acc[c][2 * i]);
                   acc[c][2 * i + 1] = __fmaf_rn(ws, bf16_hi(q[i]), acc[c][2 * i + 1]);
                 } else {
@@ -134,29 +184,51 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine(CombineArgs a) {
       }
 #pragma unroll
       for (int c = 0; c < kChunks; ++c) {
-        const int ch = h0 + (c * 32 + lane) * 8;
+        const int ch = h0 + (c * 32 + lane) * kLaneCh;
         if (ch < h_end) {
-          const uint4 o = make_uint4(pack_bf16x2(acc[c][0], acc[c][1]), pack_bf16x2(acc[c][2], acc[c][3]),
-                                     pack_bf16x2(acc[c][4], acc[c][5]), pack_bf16x2(acc[c][6], acc[c][7]));
-          st_na(out + ch, o);
+#pragma unroll
+          for (int half = 0; half < kLaneCh / 8; ++half) {
+            const float* f = acc[c] + 8 * half;
+            const uint4 o = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                                       pack_bf16x2(f[6], f[7]));
+            st_na(out + ch + 8 * half, o);
+          }
         }
       }
     }
   }
 }
 
-void launch_combine(const CombineArgs& a, bool low_latency, int blocks, cudaStream_t stream) {
-  if (low_latency)
-    (void)launch_kernel(k_combine<true>, dim3(blocks), dim3(kCombineThreads), 0, stream, a);
-  else
-    (void)launch_kernel(k_combine<false>, dim3(blocks), dim3(kCombineThreads), 0, stream, a);
+namespace {
+const void* combine_fn(int src, bool fp8) {
+  if (src == kSrcRanks)
+    return fp8 ? reinterpret_cast<const void*>(k_combine<kSrcRanks, true>)
+               : reinterpret_cast<const void*>(k_combine<kSrcRanks, false>);
+  if (src == kSrcLowLatency) return reinterpret_cast<const void*>(k_combine<kSrcLowLatency, false>);
+  return reinterpret_cast<const void*>(k_combine<kSrcExpertMajor, false>);
+}
+}  // namespace
+
+size_t combine_smem_bytes(int src, int R, int E) {
+  return src == kSrcRanks ? 4 * static_cast<size_t>(R + 1) : src == kSrcExpertMajor ? 4 * static_cast<size_t>(E + 1) : 0;
+}
+
+void launch_combine(const CombineArgs& a, int src, bool fp8, int blocks, cudaStream_t stream) {
+  const size_t smem = combine_smem_bytes(src, a.R, a.E);
+  if (src == kSrcRanks) {
+    if (fp8)
+      (void)launch_kernel(k_combine<kSrcRanks, true>, dim3(blocks), dim3(kCombineThreads), smem, stream, a);
+    else
+      (void)launch_kernel(k_combine<kSrcRanks, false>, dim3(blocks), dim3(kCombineThreads), smem, stream, a);
+  } else if (src == kSrcLowLatency) {
+    (void)launch_kernel(k_combine<kSrcLowLatency, false>, dim3(blocks), dim3(kCombineThreads), smem, stream, a);
+  } else {
+    (void)launch_kernel(k_combine<kSrcExpertMajor, false>, dim3(blocks), dim3(kCombineThreads), smem, stream, a);
+  }
 }
 
 int combine_threads() { return kCombineThreads; }
 
-const void* combine_kernel(bool low_latency) {
-  return low_latency ? reinterpret_cast<const void*>(k_combine<true>)
-                     : reinterpret_cast<const void*>(k_combine<false>);
-}
+const void* combine_kernel(int src, bool fp8) { return combine_fn(src, fp8); }
 
 }  // namespace ep

@@ -164,6 +164,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
   return false;
 }
 
+// Expert id i of a top-k table held as int64 (ids32 == 0) or int32.
+__device__ __forceinline__ long long load_topk_id(const void* topk_idx, long long i, int ids32) {
+  return ids32 ? static_cast<long long>(static_cast<const int*>(topk_idx)[i])
+               : static_cast<const long long*>(topk_idx)[i];
+}
+
 // global -> shared, completing `bytes` transaction bytes on `bar`.
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
   asm volatile(

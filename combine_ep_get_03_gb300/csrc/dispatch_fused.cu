@@ -1,0 +1,538 @@
+// Routing and dispatch in one cooperative launch on sm_103a (get_dispatch_layout
+// + dispatch, and low_latency_dispatch, of "DeepEP 要約" (stakiran.github.io)
+// section 3).
+//
+// One persistent block per SM owns a contiguous run of tokens.  Its producer
+// warp starts streaming those tokens' rows into the shared-memory stage ring
+// at once -- the rows do not depend on the routing.  Meanwhile the consumer
+// warps rank the block's tokens:
+//   normal       -- per (token, destination rank): one lane per token, the
+//                   token's ranks as a 64-bit mask (R <= 64), one ballot per
+//                   distinct rank in a 32-token batch; expert counts by
+//                   shared-memory atomics;
+//   low latency  -- per (token, k) entry and expert: __match_any_sync within a
+//                   32-entry batch, per-warp running counts in shared memory.
+// Each block publishes its counts, all blocks meet at one bounded grid
+// barrier (co-residency guaranteed by the cooperative launch), and each block
+// sums its predecessors' counts into exclusive prefixes (block 0 also forms
+// the totals).  The destination rows are then known and the consumer warps
+// quantise / store the rows exactly as k_scatter does.  Rows and slots come
+// out identical to the separate routing kernels: (source rank, token) order
+// per rank, (source rank, token, k) order per expert.
+#include <climits>
+
+#include "ep_internal.h"
+#include "scatter_common.cuh"
+
+namespace ep {
+
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+  asm volatile("bar.sync 1, %0;" : : "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" : : "l"(p), "r"(v) : "memory");
+}
+
+// Grid-wide barrier among the consumer warps of all blocks.  Word 0 counts
+// arrivals, word 1 is the generation; the last arrival resets the count and
+// bumps the generation.  Bounded: gives up after kSpinLimit polls (latched
+// kErrTimeout).
+__device__ inline void grid_sync(unsigned* words, unsigned nblocks, int* err, int nthreads) {
+  __threadfence();
+  consumer_sync(nthreads);
+  if (threadIdx.x == 32) {
+    const unsigned g = ld_acquire_u32(words + 1);
+    const unsigned arrived = atomicAdd(words, 1u);
+    if (arrived == nblocks - 1) {
+      atomicExch(words, 0u);
+      __threadfence();
+      st_release_u32(words + 1, g + 1);
+    } else {
+      int it = 0;
+      while (ld_acquire_u32(words + 1) == g) {
+        if (++it > kSpinLimit) {
+          latch_error(err, kErrTimeout);
+          break;
+        }
+        if (it > 16) __nanosleep(64);
+      }
+    }
+    __threadfence();
+  }
+  consumer_sync(nthreads);
+}
+
+__host__ __device__ inline int fused_tokens_per_block(int T, int nb) { return (T + nb - 1) / nb; }
+
+// Column `col` of the per-block counts summed over blocks q < b (exclusive)
+// and over all blocks.  Loads are issued 32 at a time before any is added, so
+// a column costs one L2 round trip per 32 blocks.
+__device__ __forceinline__ void column_sums(const int* agg, int NK, int col, int nb, int b, int* ex, int* all) {
+  int e = 0, a = 0;
+  for (int q0 = 0; q0 < nb; q0 += 32) {
+    int v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = q0 + j < nb ? __ldcg(agg + static_cast<size_t>(q0 + j) * NK + col) : 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      a += v[j];
+      if (q0 + j < b) e += v[j];
+    }
+  }
+  *ex = e;
+  *all = a;
+}
+
+// Routing tables in shared memory (int32 unless noted).
+__host__ __device__ inline size_t fused_route_bytes(bool low_latency, int R, int E, int kmax, int kp, int tpb, int nc) {
+  if (!low_latency)
+    return 8 * static_cast<size_t>(tpb)                        // token rank masks (u64)
+           + 8 * static_cast<size_t>(tpb) * kmax               // (rank, row) per token
+           + 4 * static_cast<size_t>(tpb) * kmax               // local rows
+           + 4 * (static_cast<size_t>(nc) * R + E + 3 * (R + 1) + 4);
+  const size_t ni = static_cast<size_t>(tpb) * kp;
+  return 8 * ni + 4 * (static_cast<size_t>(nc) * E + E + 4);
+}
+
+__host__ __device__ inline size_t fused_smem_bytes(bool low_latency, bool fp8, int R, int E, int kmax, int kp,
+                                                   int tpb, int nc, int ns, int H) {
+  const size_t route = (fused_route_bytes(low_latency, R, E, kmax, kp, tpb, nc) + 127) & ~static_cast<size_t>(127);
+  const size_t qb = static_cast<size_t>(H) + ((4 * static_cast<size_t>(H / 128) + 15) & ~15ull);
+  return route + 16 * static_cast<size_t>(ns) + static_cast<size_t>(ns) * 2 * H + (fp8 ? nc * qb : 0);
+}
+
+template <bool kFP8, bool kLL>
+__global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_scatter(FusedArgs a, int NS) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int NC = (blockDim.x >> 5) - 1;
+  const int nct = NC * 32;  // consumer threads
+  const int ct = threadIdx.x - 32;
+  const int R = a.R, E = a.E, k = a.k, kmax = a.kmax, kp = 1 << a.kp_log2;
+  const int H = a.H;
+  const int G = H >> 7;
+  const uint32_t row_bytes = 2u * static_cast<uint32_t>(H);
+  const int nb = gridDim.x;
+  const int b = blockIdx.x;
+  const int tpb = fused_tokens_per_block(a.T, nb);
+  const int t_begin = min(a.T, b * tpb);
+  const int n_own = min(a.T, t_begin + tpb) - t_begin;
+
+  // ---- shared memory carve-up
+  unsigned char* p = smem;
+  unsigned long long* tmask = nullptr;
+  int2* tdst = nullptr;
+  int *tlocal = nullptr, *cnt = nullptr, *hist = nullptr, *so = nullptr, *excl = nullptr, *tot = nullptr;
+  int *item_e = nullptr, *item_slot = nullptr;
+  if (!kLL) {
+    tmask = reinterpret_cast<unsigned long long*>(p);
+    p += 8 * static_cast<size_t>(tpb);
+    tdst = reinterpret_cast<int2*>(p);
+    p += 8 * static_cast<size_t>(tpb) * kmax;
+    tlocal = reinterpret_cast<int*>(p);
+    p += 4 * static_cast<size_t>(tpb) * kmax;
+    cnt = reinterpret_cast<int*>(p);   // [NC][R]
+    hist = cnt + NC * R;               // [E]
+    so = hist + E;                     // [R+1] rank_offset
+    excl = so + (R + 1);               // [R+1]
+    tot = excl + (R + 1);              // [R+1]
+  } else {
+    item_e = reinterpret_cast<int*>(p);
+    item_slot = item_e + tpb * kp;
+    cnt = item_slot + tpb * kp;        // [NC][E], then per-warp prefixes
+    excl = cnt + NC * E;               // [E]
+  }
+  unsigned char* sbase = smem + ((fused_route_bytes(kLL, R, E, kmax, kp, tpb, NC) + 127) & ~static_cast<size_t>(127));
+  uint64_t* full = reinterpret_cast<uint64_t*>(sbase);
+  uint64_t* empty = full + NS;
+  unsigned char* stage0 = reinterpret_cast<unsigned char*>(empty + NS);
+  unsigned char* qbuf0 = stage0 + static_cast<size_t>(NS) * row_bytes;
+  auto stage = [&](int s) { return stage0 + static_cast<size_t>(s) * row_bytes; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    mbar_init_fence();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // producer: the block's rows, in order, from the first instruction on
+    if (lane == 0) {
+      for (int i = 0; i < n_own; ++i) {
+        const int s = i % NS;
+        if (i >= NS && !mbar_wait(empty + s, static_cast<uint32_t>((i / NS - 1) & 1), a.err)) break;
+        mbar_arrive_expect_tx(full + s, row_bytes);
+        bulk_load(stage(s), a.x + static_cast<size_t>(t_begin + i) * H, row_bytes, full + s);
+      }
+    }
+    return;
+  }
+
+  const int cw = warp - 1;  // consumer warp
+  const unsigned lt = lanemask_lt();
+  // ---------------------------------------------------------------- phase 1: rank the block's tokens
+  if (!kLL) {
+    for (int i = ct; i < E; i += nct) hist[i] = 0;
+    consumer_sync(nct);
+    const int tpw = ((tpb + NC - 1) / NC + 31) & ~31;
+    int run_lo = 0, run_hi = 0;
+    for (int b0 = cw * tpw; b0 < min(n_own, (cw + 1) * tpw); b0 += 32) {  // warp-uniform
+      const int tl = b0 + lane;
+      const bool live = tl < n_own && tl < (cw + 1) * tpw;
+      unsigned long long m = 0;
+      if (live) {
+        const int t = t_begin + tl;
+        const long long ids = static_cast<long long>(t) * k;
+        for (int j0 = 0; j0 < k; j0 += 8) {
+          long long v[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] = j0 + j < k ? load_topk_id(a.topk_idx, ids + j0 + j, a.ids32) : -1;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (j0 + j >= k) break;
+            long long e = v[j];
+            if (e < -1 || e >= E) {
+              latch_error(a.err, kErrBadExpert);
+              e = -1;
+            }
+            a.idx32[static_cast<size_t>(t) * k + j0 + j] = static_cast<int>(e);
+            if (e >= 0) {
+              m |= 1ull << (static_cast<int>(e) / a.El);
+              atomicAdd(hist + static_cast<int>(e), 1);
+            }
+          }
+        }
+        tmask[tl] = m;
+      }
+      unsigned long long present =
+          static_cast<unsigned long long>(__reduce_or_sync(kFullMask, static_cast<unsigned>(m))) |
+          (static_cast<unsigned long long>(__reduce_or_sync(kFullMask, static_cast<unsigned>(m >> 32))) << 32);
+      while (present) {  // warp-uniform: ascending ranks present in this batch
+        const int r = __ffsll(static_cast<long long>(present)) - 1;
+        present &= present - 1;
+        const bool has = (m >> r) & 1ull;
+        const unsigned bal = __ballot_sync(kFullMask, has);
+        const int base = __shfl_sync(kFullMask, r < 32 ? run_lo : run_hi, r & 31);
+        if (has) tlocal[tl * kmax + __popcll(m & ((1ull << r) - 1ull))] = base + __popc(bal & lt);
+        if (lane == (r & 31)) {
+          if (r < 32) run_lo += __popc(bal);
+          else run_hi += __popc(bal);
+        }
+      }
+    }
+    if (lane < R) cnt[cw * R + lane] = run_lo;
+    if (lane + 32 < R) cnt[cw * R + lane + 32] = run_hi;
+    consumer_sync(nct);
+    for (int col = ct; col < R; col += nct) {
+      int run = 0;
+      for (int w = 0; w < NC; ++w) {
+        const int v = cnt[w * R + col];
+        cnt[w * R + col] = run;
+        run += v;
+      }
+      a.agg[static_cast<size_t>(b) * (R + E) + col] = run;
+    }
+    for (int e = ct; e < E; e += nct) a.agg[static_cast<size_t>(b) * (R + E) + R + e] = hist[e];
+  } else {
+    const int NI = tpb << a.kp_log2;
+    const int ipw = (((NI + NC - 1) / NC) + 31) & ~31;
+    for (int i = ct; i < NC * E; i += nct) cnt[i] = 0;
+    consumer_sync(nct);
+    int* cntw = cnt + cw * E;
+    for (int b0 = cw * ipw; b0 < min(NI, (cw + 1) * ipw); b0 += 32) {  // warp-uniform
+      const int i = b0 + lane;
+      const int tl = i >> a.kp_log2;
+      const int j = i & (kp - 1);
+      const bool in_blk = i < (cw + 1) * ipw && tl < n_own;
+      int e = -1;
+      if (in_blk && j < k) {
+        long long v = load_topk_id(a.topk_idx, static_cast<long long>(t_begin + tl) * k + j, a.ids32);
+        if (v < -1 || v >= E) {
+          latch_error(a.err, kErrBadExpert);
+          v = -1;
+        }
+        e = static_cast<int>(v);
+      }
+      const unsigned pe = __match_any_sync(kFullMask, e);
+      int le = 0;
+      if (e >= 0) le = cntw[e] + __popc(pe & lt);
+      __syncwarp();
+      if (e >= 0 && lane == __ffs(pe) - 1) cntw[e] += __popc(pe);
+      __syncwarp();
+      if (i < NI) {
+        item_e[i] = e;
+        item_slot[i] = le;
+      }
+    }
+    consumer_sync(nct);
+    for (int col = ct; col < E; col += nct) {
+      int run = 0;
+      for (int w = 0; w < NC; ++w) {
+        const int v = cnt[w * E + col];
+        cnt[w * E + col] = run;
+        run += v;
+      }
+      a.agg[static_cast<size_t>(b) * E + col] = run;
+    }
+  }
+
+  // ---------------------------------------------------------------- phase 2: prefixes over blocks
+  grid_sync(a.barrier, static_cast<unsigned>(nb), a.err, nct);
+  const int NK = kLL ? E : R + E;
+  if (!kLL) {
+    for (int col = ct; col < R; col += nct) column_sums(a.agg, NK, col, nb, b, excl + col, tot + col);
+    consumer_sync(nct);
+    if (cw == 0) {  // exclusive scan of the rank totals -> region offsets
+      const int v = lane < R ? tot[lane] : 0;
+      const int v2 = lane + 32 < R ? tot[lane + 32] : 0;
+      int inc = v, inc2 = v2;
+      for (int d = 1; d < 32; d <<= 1) {
+        const int u = __shfl_up_sync(kFullMask, inc, d);
+        const int u2 = __shfl_up_sync(kFullMask, inc2, d);
+        if (lane >= d) {
+          inc += u;
+          inc2 += u2;
+        }
+      }
+      const int carry = __shfl_sync(kFullMask, inc, 31);
+      const int total2 = __shfl_sync(kFullMask, inc2, 31);
+      if (lane < R) so[lane] = inc - v;
+      if (lane + 32 < R) so[lane + 32] = carry + inc2 - v2;
+      if (lane == 0) so[R] = carry + total2;
+      if (b == 0) {
+        if (lane < R) {
+          a.rank_offset[lane] = inc - v;
+          a.recv_per_rank[lane] = v;
+        }
+        if (lane + 32 < R) {
+          a.rank_offset[lane + 32] = carry + inc2 - v2;
+          a.recv_per_rank[lane + 32] = v2;
+        }
+        if (lane == 0) a.rank_offset[R] = carry + total2;
+      }
+    }
+    consumer_sync(nct);
+    // each token's (rank, row-in-rank) list for the handle, and its global rows here
+    const int tpw = ((tpb + NC - 1) / NC + 31) & ~31;
+    for (int tl = ct; tl < n_own; tl += nct) {
+      const int t = t_begin + tl;
+      const int w = tl / tpw;
+      unsigned long long m = tmask[tl];
+      int pos = 0;
+      while (m) {
+        const int r = __ffsll(static_cast<long long>(m)) - 1;
+        m &= m - 1;
+        const int in_rank = excl[r] + cnt[w * R + r] + tlocal[tl * kmax + pos];
+        a.dst[static_cast<size_t>(t) * kmax + pos] = make_int2(r, in_rank);
+        tdst[tl * kmax + pos] = make_int2(r, so[r] + in_rank);
+        ++pos;
+      }
+      for (; pos < kmax; ++pos) {
+        a.dst[static_cast<size_t>(t) * kmax + pos] = make_int2(-1, -1);
+        tdst[tl * kmax + pos] = make_int2(-1, -1);
+      }
+    }
+  } else {
+    for (int col = ct; col < E; col += nct) {
+      int all;
+      column_sums(a.agg, NK, col, nb, b, excl + col, &all);
+    }
+    consumer_sync(nct);
+    const int NI = tpb << a.kp_log2;
+    const int ipw = (((NI + NC - 1) / NC) + 31) & ~31;
+    for (int i = ct; i < n_own * kp; i += nct) {
+      const int tl = i >> a.kp_log2;
+      const int j = i & (kp - 1);
+      if (j >= k) continue;
+      const int t = t_begin + tl;
+      const int e = item_e[i];
+      int slot = -1;
+      if (e >= 0) {
+        slot = excl[e] + cnt[(i / ipw) * E + e] + item_slot[i];
+        if (slot >= a.M) {
+          latch_error(a.err, kErrCapacity);
+          slot = -1;
+        }
+      }
+      a.ll_idx[static_cast<size_t>(t) * k + j] = e;
+      a.ll_slot[static_cast<size_t>(t) * k + j] = slot;
+      item_slot[i] = slot;
+    }
+  }
+  consumer_sync(nct);
+
+  // ---------------------------------------------------------------- phase 3: move the rows
+  unsigned char* qd = qbuf0 + static_cast<size_t>(cw) * (static_cast<size_t>(H) + ((4 * G + 15) & ~15));
+  float* sd = reinterpret_cast<float*>(qd + H);
+  const bool meta = !kLL && (a.recv_src_idx || a.recv_topk_idx || a.recv_topk_weights);
+  bool first = true;
+  for (int i = cw; i < n_own; i += NC) {
+    const int t = t_begin + i;
+    const int s = i % NS;
+    long long row = -1;
+    int r = -1, e = -1;
+    float w = 0.0f;
+    if (!kLL) {
+      if (lane < kmax) {
+        const int2 d = tdst[i * kmax + lane];
+        if (d.x >= 0) {
+          r = d.x;
+          row = d.y;
+          if (row >= a.cap) {
+            latch_error(a.err, kErrCapacity);
+            row = -1;
+          }
+        }
+      }
+      if (meta && lane < k) {
+        e = a.idx32[static_cast<size_t>(t) * k + lane];
+        if (a.topk_weights) w = a.topk_weights[static_cast<size_t>(t) * k + lane];
+      }
+    } else if (lane < k) {
+      const int ee = item_e[(i << a.kp_log2) + lane];
+      const int sl = item_slot[(i << a.kp_log2) + lane];
+      if (ee >= 0 && sl >= 0) row = static_cast<long long>(ee) * a.M + sl;
+    }
+    const unsigned dmask = __ballot_sync(kFullMask, row >= 0);
+    const bool landed = mbar_wait(full + s, static_cast<uint32_t>((i / NS) & 1), a.err);
+    if (!__all_sync(kFullMask, landed)) break;
+    if (kFP8) {
+      if (!first) {
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+      }
+      quantize_row_smem(stage(s), qd, sd, G, lane);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + s);
+      unsigned m = dmask;
+      while (m) {
+        const int sl = __ffs(m) - 1;
+        m &= m - 1;
+        const long long rr = __shfl_sync(kFullMask, row, sl);
+        if (lane == 0) bulk_store(static_cast<uint8_t*>(a.recv_x) + rr * H, qd, static_cast<uint32_t>(H));
+        for (int g = lane; g < G; g += 32) a.recv_scales[rr * G + g] = sd[g];
+      }
+      if (lane == 0) bulk_commit();
+    } else {
+      unsigned m = dmask;
+      while (m) {
+        const int sl = __ffs(m) - 1;
+        m &= m - 1;
+        const long long rr = __shfl_sync(kFullMask, row, sl);
+        if (lane == 0) bulk_store(static_cast<uint16_t*>(a.recv_x) + rr * H, stage(s), row_bytes);
+      }
+      if (lane == 0) {
+        bulk_commit();
+        bulk_wait_read<0>();
+        mbar_arrive(empty + s);
+      }
+      __syncwarp();
+    }
+    first = false;
+    if (meta) {
+      unsigned m = dmask;
+      while (m) {
+        const int sl = __ffs(m) - 1;
+        m &= m - 1;
+        const long long rr = __shfl_sync(kFullMask, row, sl);
+        const int rk = __shfl_sync(kFullMask, r, sl);
+        if (lane == 0 && a.recv_src_idx) a.recv_src_idx[rr] = t;
+        if (lane < k) {
+          const bool here = e >= 0 && e / a.El == rk;
+          if (a.recv_topk_idx) a.recv_topk_idx[rr * k + lane] = here ? e - rk * a.El : -1;
+          if (a.recv_topk_weights) a.recv_topk_weights[rr * k + lane] = here ? w : 0.0f;
+        }
+      }
+    } else if (kLL && a.recv_src_info && row >= 0) {
+      a.recv_src_info[row] = t;
+    }
+  }
+  // per-expert totals (outputs only, nothing above waits for them): block b
+  // forms the totals of experts e = b, b + nb, ...
+  for (int e = b + ct * nb; e < E; e += nct * nb) {
+    int ex, all;
+    column_sums(a.agg, NK, (kLL ? 0 : R) + e, nb, 0, &ex, &all);
+    if (kLL) {
+      if (a.recv_count) a.recv_count[e] = min(all, a.M);
+    } else {
+      a.recv_per_expert[e] = all;
+    }
+  }
+  if (lane == 0) bulk_wait_all();
+  __syncwarp();
+}
+
+// Blocks, stages and consumers for the fused kernel; blocks = 0 when it does
+// not apply (R > 64 in normal mode, too many (token, k) entries per block,
+// rows too long for two stages).
+void fused_config(bool low_latency, bool fp8, int T, int R, int E, int k, int kmax, int H, int sms,
+                  size_t smem_limit, int* blocks, int* NS, int* NC) {
+  *blocks = *NS = *NC = 0;
+  if (T <= 0 || (!low_latency && R > 64)) return;
+  int kp = 1;
+  while (kp < k) kp <<= 1;
+  const int nb = sms;
+  const int tpb = fused_tokens_per_block(T, nb);
+  if (tpb * kp > kFusedMaxItems) return;
+  for (int nc = fp8 ? kScatterMaxConsumers : 4; nc >= 1; --nc) {
+    const size_t fixed = fused_smem_bytes(low_latency, fp8, R, E, kmax, kp, tpb, nc, 0, H);
+    if (fixed >= smem_limit) continue;
+    int ns = static_cast<int>((smem_limit - fixed) / (16 + 2 * static_cast<size_t>(H)));
+    if (ns > 32) ns = 32;
+    if (ns >= 2) {
+      *blocks = nb;
+      *NS = ns;
+      *NC = nc;
+      return;
+    }
+  }
+}
+
+cudaError_t configure_fused(size_t smem_limit) {
+  const void* ks[4] = {reinterpret_cast<const void*>(k_route_scatter<false, false>),
+                       reinterpret_cast<const void*>(k_route_scatter<true, false>),
+                       reinterpret_cast<const void*>(k_route_scatter<false, true>),
+                       reinterpret_cast<const void*>(k_route_scatter<true, true>)};
+  for (const void* kk : ks) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_limit));
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_fused(const FusedArgs& a, bool fp8, bool low_latency, int blocks, int NS, int NC,
+                         cudaStream_t stream) {
+  int kp = 1;
+  while (kp < a.k) kp <<= 1;
+  const int tpb = fused_tokens_per_block(a.T, blocks);
+  const size_t smem = fused_smem_bytes(low_latency, fp8, a.R, a.E, a.kmax, kp, tpb, NC, NS, a.H);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3((NC + 1) * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (low_latency)
+    return fp8 ? cudaLaunchKernelEx(&cfg, k_route_scatter<true, true>, a, NS)
+               : cudaLaunchKernelEx(&cfg, k_route_scatter<false, true>, a, NS);
+  return fp8 ? cudaLaunchKernelEx(&cfg, k_route_scatter<true, false>, a, NS)
+             : cudaLaunchKernelEx(&cfg, k_route_scatter<false, false>, a, NS);
+}
+
+}  // namespace ep

@@ -69,25 +69,32 @@ void launch_dispatch(const DispatchArgs& a, bool fp8, int blocks, cudaStream_t s
 int dispatch_threads();
 const void* dispatch_kernel(bool fp8);
 
-// Normal and low-latency combine: one warp per token.
+// combine: one warp per (token, 1024-channel part), every receive layout.
+enum : int { kSrcRanks = 0, kSrcLowLatency = 1, kSrcExpertMajor = 2 };
 struct CombineArgs {
-  const uint16_t* y;           // rows of bf16 [.][H]
+  const void* y;               // rows [.][H]: bf16, or e4m3 bytes with y_scales
+  const float* y_scales;       // [y_rows][H/128] (e4m3 rows)
   uint16_t* out;               // [T][H]
   long long y_rows;
-  int T, H, k, kmax, R;
-  // normal mode
+  int T, H, k, kmax, R, E;
+  // rank-major (normal) rows
   const int2* dst;             // [T][kmax]
   const int* rank_offset;      // [R+1]
-  // low-latency mode
-  const int* ll_idx;           // [T][k]
-  const int* ll_slot;          // [T][k]
-  const float* topk_weights;   // [T][k]
-  int M;
+  const float* recv_topk_weights;  // [y_rows][k] or null
+  float* combined_topk_weights;    // [T][k] (with recv_topk_weights)
+  // low-latency / expert-major rows: per (token, k) entry its expert id and
+  // its slot inside the expert
+  const int* ent_idx;          // [T][k]
+  const int* ent_slot;         // [T][k]
+  const float* topk_weights;   // [T][k] (low latency)
+  int M;                       // low latency: rows per expert
+  const int* expert_offset;    // expert-major: [E+1] first row of each expert
   int* err;
 };
-void launch_combine(const CombineArgs& a, bool low_latency, int blocks, cudaStream_t stream);
+void launch_combine(const CombineArgs& a, int src, bool fp8, int blocks, cudaStream_t stream);
+size_t combine_smem_bytes(int src, int R, int E);
 int combine_threads();
-const void* combine_kernel(bool low_latency);
+const void* combine_kernel(int src, bool fp8);
 
 // TMA bulk-copy scatter (dispatch row movement), persistent: one block per
 // SM, one producer warp and up to kScatterMaxConsumers consumer warps.
@@ -121,6 +128,42 @@ size_t scatter_smem_bytes(int H, int R, bool fp8, bool low_latency, int NS, int 
 cudaError_t configure_scatter(size_t smem_limit);
 void launch_scatter(const ScatterArgs& a, bool fp8, bool low_latency, int blocks, int NS, int NC,
                     cudaStream_t stream);
+
+// Fused routing + dispatch (cooperative launch, one block per SM).
+constexpr int kFusedMaxItems = 4096;  // (token, k) entries a block may own
+struct FusedArgs {
+  const void* topk_idx;        // [T][k] int64, or int32 if ids32
+  int ids32;
+  const uint16_t* x;
+  const float* topk_weights;
+  int T, R, E, El, k, kp_log2, kmax, H, M;
+  int* agg;           // [blocks][R+E] (normal) or [blocks][E] (low latency)
+  unsigned* barrier;  // [2] grid barrier words
+  int* err;
+  // normal mode: the handle's layout state and the dispatch outputs
+  int2* dst;
+  int* idx32;
+  int* recv_per_rank;
+  int* rank_offset;
+  int* recv_per_expert;
+  long long cap;
+  int* recv_src_idx;
+  int* recv_topk_idx;
+  float* recv_topk_weights;
+  // low-latency mode
+  int* ll_idx;
+  int* ll_slot;
+  int* recv_count;
+  int* recv_src_info;
+  // rows
+  void* recv_x;
+  float* recv_scales;
+};
+void fused_config(bool low_latency, bool fp8, int T, int R, int E, int k, int kmax, int H, int sms,
+                  size_t smem_limit, int* blocks, int* NS, int* NC);
+cudaError_t configure_fused(size_t smem_limit);
+cudaError_t launch_fused(const FusedArgs& a, bool fp8, bool low_latency, int blocks, int NS, int NC,
+                         cudaStream_t stream);
 
 // Low-latency routing only (slots, counts); the rows move with k_scatter.
 void launch_ll_route(const RouteParams& p, const LowLatencyOutPtrs& o, size_t smem, cudaStream_t stream);

@@ -170,11 +170,11 @@ __global__ void __launch_bounds__(kRouteThreads) k_layout_tokens(RouteParams p, 
     const bool live = tl < ct && tl < (warp + 1) * tpw;
     unsigned long long m = 0;
     if (live) {
-      const int64_t* ids = p.topk_idx + static_cast<long long>(t0 + tl) * k;
+      const long long ids = static_cast<long long>(t0 + tl) * k;
       for (int j0 = 0; j0 < k; j0 += 8) {
         long long v[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = j0 + j < k ? ids[j0 + j] : -1;
+        for (int j = 0; j < 8; ++j) v[j] = j0 + j < k ? load_topk_id(p.topk_idx, ids + j0 + j, p.ids32) : -1;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           if (j0 + j >= k) break;

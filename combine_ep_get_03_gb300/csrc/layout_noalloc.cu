@@ -112,6 +112,7 @@ extern "C" ep_status_t ep_get_dispatch_layout_noalloc(int R, int E, int k, const
 
   ep::RouteParams p;
   p.topk_idx = topk_idx;
+  p.ids32 = 0;
   p.T = T;
   p.R = R;
   p.E = E;

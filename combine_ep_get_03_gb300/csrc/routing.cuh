@@ -33,7 +33,8 @@ constexpr int kRouteThreads = 256;
 constexpr int kRouteWarps = kRouteThreads / 32;
 
 struct RouteParams {
-  const int64_t* topk_idx;  // [T][k]
+  const void* topk_idx;     // [T][k], int64 or int32 (ids32)
+  int ids32;
   int T, R, E, El, k;
   int kp_log2;              // lanes per token: the power of two >= k
   int kmax;                 // min(k, R): distinct ranks a token can reach
@@ -117,7 +118,7 @@ __device__ inline void route_rank_chunk(const RouteParams& p, const RouteSmem& s
     const int i = begin + bb * 32 + lane;
     const int tl = i >> p.kp_log2;
     const int j = i & (kp - 1);
-    pre[bb] = (i < end && tl < ct && j < p.k) ? p.topk_idx[static_cast<long long>(t0 + tl) * p.k + j] : -1;
+    pre[bb] = (i < end && tl < ct && j < p.k) ? load_topk_id(p.topk_idx, static_cast<long long>(t0 + tl) * p.k + j, p.ids32) : -1;
   }
   for (int i = threadIdx.x; i < kRouteWarps * NK; i += kRouteThreads) s.cnt[i] = 0;
   __syncthreads();

@@ -48,6 +48,11 @@ def lib() -> ctypes.CDLL:
             L.ep_get_num_recv.argtypes = [P, P, P, P, P]
             L.ep_dispatch.argtypes = [P, P, P, I, P, P, I64, P, P, P, I, P]
             L.ep_combine.argtypes = [P, P, I64, P, I, P]
+            L.ep_combine_ex.argtypes = [P, I, P, P, I64, P, P, P, I, P]
+            L.ep_handle_set_topk_idx_bits.argtypes = [P, I]
+            L.ep_handle_topk_idx_bits.argtypes = [P]
+            L.ep_handle_topk_idx_bits.restype = I
+            L.ep_layout_and_dispatch.argtypes = [P, P, I, P, P, I, P, P, I64, P, P, P, I, P]
             L.ep_low_latency_dispatch.argtypes = [P, P, P, I, I, P, P, P, P, I, P]
             L.ep_low_latency_combine.argtypes = [P, P, P, P, I, P]
             L.ep_get_device_status.argtypes = [P, P]
@@ -55,7 +60,8 @@ def lib() -> ctypes.CDLL:
             L.ep_status_str.argtypes = [I]
             L.ep_status_str.restype = ctypes.c_char_p
             for n in ("ep_handle_create", "ep_handle_destroy", "ep_get_dispatch_layout", "ep_get_num_recv",
-                      "ep_dispatch", "ep_combine", "ep_low_latency_dispatch", "ep_low_latency_combine",
+                      "ep_dispatch", "ep_combine", "ep_layout_and_dispatch", "ep_low_latency_dispatch",
+                      "ep_low_latency_combine", "ep_combine_ex", "ep_handle_set_topk_idx_bits",
                       "ep_get_device_status", "ep_get_dispatch_layout_noalloc"):
                 getattr(L, n).restype = I
             _lib = L
@@ -100,6 +106,12 @@ def _ptr(t, dtypes=None, name="tensor"):
 _FP8_BYTES = (torch.uint8, torch.float8_e4m3fn)
 
 
+def _ids_ptr(h, topk_idx):
+    """topk_idx must have the width the handle reads (int64 or int32)."""
+    bits = lib().ep_handle_topk_idx_bits(h)
+    return _ptr(topk_idx, (torch.int32,) if bits == 32 else (torch.int64,), "topk_idx")
+
+
 # ------------------------------------------------------------------ calls
 
 def ep_handle_create(num_ranks: int, num_experts: int, num_topk: int, hidden: int,
@@ -110,6 +122,14 @@ def ep_handle_create(num_ranks: int, num_experts: int, num_topk: int, hidden: in
     return h.value
 
 
+def ep_handle_set_topk_idx_bits(h: int, bits: int) -> None:
+    _check(lib().ep_handle_set_topk_idx_bits(h, int(bits)), "ep_handle_set_topk_idx_bits")
+
+
+def ep_handle_topk_idx_bits(h: int) -> int:
+    return int(lib().ep_handle_topk_idx_bits(h))
+
+
 def ep_handle_destroy(h: int) -> None:
     _check(lib().ep_handle_destroy(h), "ep_handle_destroy")
 
@@ -118,7 +138,7 @@ def ep_get_dispatch_layout(h, topk_idx, num_tokens_per_rank=None, num_tokens_per
                            is_token_in_rank=None, stream=None) -> None:
     T = topk_idx.shape[0]
     _check(lib().ep_get_dispatch_layout(
-        h, _ptr(topk_idx, (torch.int64,), "topk_idx"), T,
+        h, _ids_ptr(h, topk_idx), T,
         _ptr(num_tokens_per_rank, (torch.int32,), "num_tokens_per_rank"),
         _ptr(num_tokens_per_expert, (torch.int32,), "num_tokens_per_expert"),
         _ptr(is_token_in_rank, (torch.bool, torch.uint8), "is_token_in_rank"),
@@ -151,16 +171,43 @@ def ep_dispatch(h, x, topk_weights, dtype: int, recv_x, recv_scales=None, recv_s
         int(num_sms), _stream(stream)), "ep_dispatch")
 
 
+def ep_layout_and_dispatch(h, topk_idx, x, topk_weights, dtype: int, recv_x, recv_scales=None, recv_src_idx=None,
+                           recv_topk_idx=None, recv_topk_weights=None, num_sms: int = 0, stream=None) -> None:
+    fp8 = dtype == EP_FP8_E4M3
+    cap = recv_x.shape[0] if recv_x is not None else 0
+    _check(lib().ep_layout_and_dispatch(
+        h, _ids_ptr(h, topk_idx), topk_idx.shape[0], _ptr(x, (torch.bfloat16,), "x"),
+        _ptr(topk_weights, (torch.float32,), "topk_weights"), int(dtype),
+        _ptr(recv_x, _FP8_BYTES if fp8 else (torch.bfloat16,), "recv_x"),
+        _ptr(recv_scales, (torch.float32,), "recv_scales") if fp8 else None, cap,
+        _ptr(recv_src_idx, (torch.int32,), "recv_src_idx"),
+        _ptr(recv_topk_idx, (torch.int32,), "recv_topk_idx"),
+        _ptr(recv_topk_weights, (torch.float32,), "recv_topk_weights"),
+        int(num_sms), _stream(stream)), "ep_layout_and_dispatch")
+
+
 def ep_combine(h, y, out, num_sms: int = 0, stream=None) -> None:
     _check(lib().ep_combine(h, _ptr(y, (torch.bfloat16,), "y"), y.shape[0],
                             _ptr(out, (torch.bfloat16,), "out"), int(num_sms), _stream(stream)), "ep_combine")
+
+
+def ep_combine_ex(h, y, out, y_scales=None, recv_topk_weights=None, combined_topk_weights=None, num_sms: int = 0,
+                  stream=None) -> None:
+    """y bf16 [rows, H], or e4m3 bytes [rows, H] with fp32 y_scales [rows, H/128]."""
+    fp8 = y_scales is not None
+    _check(lib().ep_combine_ex(
+        h, EP_FP8_E4M3 if fp8 else EP_BF16, _ptr(y, _FP8_BYTES if fp8 else (torch.bfloat16,), "y"),
+        _ptr(y_scales, (torch.float32,), "y_scales"), y.shape[0],
+        _ptr(recv_topk_weights, (torch.float32,), "recv_topk_weights"), _ptr(out, (torch.bfloat16,), "out"),
+        _ptr(combined_topk_weights, (torch.float32,), "combined_topk_weights"), int(num_sms), _stream(stream)),
+        "ep_combine_ex")
 
 
 def ep_low_latency_dispatch(h, x, topk_idx, dtype: int, recv_x, recv_scales=None, recv_src_info=None,
                             recv_count=None, num_sms: int = 0, stream=None) -> None:
     fp8 = dtype == EP_FP8_E4M3
     _check(lib().ep_low_latency_dispatch(
-        h, _ptr(x, (torch.bfloat16,), "x"), _ptr(topk_idx, (torch.int64,), "topk_idx"), topk_idx.shape[0],
+        h, _ptr(x, (torch.bfloat16,), "x"), _ids_ptr(h, topk_idx), topk_idx.shape[0],
         int(dtype), _ptr(recv_x, _FP8_BYTES if fp8 else (torch.bfloat16,), "recv_x"),
         _ptr(recv_scales, (torch.float32,), "recv_scales") if fp8 else None,
         _ptr(recv_src_info, (torch.int32,), "recv_src_info"), _ptr(recv_count, (torch.int32,), "recv_count"),
@@ -217,6 +264,13 @@ class Handle:
         self.T = None      # tokens of the last layout
         self.T_ll = None   # tokens of the last low-latency dispatch
         self.ptr = ep_handle_create(num_ranks, num_experts, num_topk, hidden, max_tokens_per_rank)
+
+    @property
+    def topk_idx_bits(self) -> int:
+        return ep_handle_topk_idx_bits(self.ptr)
+
+    def set_topk_idx_bits(self, bits: int) -> None:
+        ep_handle_set_topk_idx_bits(self.ptr, bits)
 
     @property
     def M(self) -> int:
@@ -283,6 +337,27 @@ class Handle:
         ep_dispatch(self.ptr, x, topk_weights, dtype, recv_x, recv_scales, recv_src_idx, recv_topk_idx,
                     recv_topk_weights, num_sms, stream)
 
+    def layout_and_dispatch(self, topk_idx, x, topk_weights, dtype, recv_x, recv_scales=None, recv_src_idx=None,
+                            recv_topk_idx=None, recv_topk_weights=None, num_sms=0, stream=None):
+        T = topk_idx.shape[0]
+        if topk_idx.dim() != 2 or topk_idx.shape[1] != self.k:
+            raise ValueError(f"topk_idx must be [T, {self.k}]")
+        cap = recv_x.shape[0]
+        if recv_x.dim() != 2 or recv_x.shape[1] != self.H:
+            raise ValueError(f"recv_x must be [cap, {self.H}]")
+        self._need(x, T * self.H, "x")
+        self._need(topk_weights, T * self.k, "topk_weights")
+        if dtype == EP_FP8_E4M3:
+            if recv_scales is None:
+                raise ValueError("FP8 dispatch needs recv_scales")
+            self._need(recv_scales, cap * self.G, "recv_scales")
+        self._need(recv_src_idx, cap, "recv_src_idx")
+        self._need(recv_topk_idx, cap * self.k, "recv_topk_idx")
+        self._need(recv_topk_weights, cap * self.k, "recv_topk_weights")
+        ep_layout_and_dispatch(self.ptr, topk_idx, x, topk_weights, dtype, recv_x, recv_scales, recv_src_idx,
+                               recv_topk_idx, recv_topk_weights, num_sms, stream)
+        self.T = T
+
     def combine(self, y, out, num_sms=0, stream=None):
         if self.T is None:
             raise RuntimeError("combine before any layout on this handle")
@@ -290,6 +365,19 @@ class Handle:
             raise ValueError(f"y must be [rows, {self.H}]")
         self._need(out, self.T * self.H, "out")
         ep_combine(self.ptr, y, out, num_sms, stream)
+
+    def combine_ex(self, y, out, y_scales=None, recv_topk_weights=None, combined_topk_weights=None, num_sms=0,
+                   stream=None):
+        if self.T is None:
+            raise RuntimeError("combine before any layout on this handle")
+        if y.dim() != 2 or y.shape[1] != self.H:
+            raise ValueError(f"y must be [rows, {self.H}]")
+        rows = y.shape[0]
+        self._need(out, self.T * self.H, "out")
+        self._need(y_scales, rows * self.G, "y_scales")
+        self._need(recv_topk_weights, rows * self.k, "recv_topk_weights")
+        self._need(combined_topk_weights, self.T * self.k, "combined_topk_weights")
+        ep_combine_ex(self.ptr, y, out, y_scales, recv_topk_weights, combined_topk_weights, num_sms, stream)
 
     def low_latency_dispatch(self, x, topk_idx, dtype, recv_x, recv_scales=None, recv_src_info=None,
                              recv_count=None, num_sms=0, stream=None):

@@ -86,13 +86,27 @@ typedef enum { EP_BF16 = 0, EP_FP8_E4M3 = 1 } ep_dtype_t;
 ep_status_t ep_handle_create(int num_ranks, int num_experts, int num_topk, int hidden,
                              int max_tokens_per_rank, ep_handle_t* out);
 
+/* Width of the top-k expert ids that the calls taking `topk_idx` read
+ * through this handle: 64 (int64, the default) or 32 (int32).  The default
+ * comes from the environment variable EP_NUM_TOPK_IDX_BITS ("64" or "32";
+ * any other value makes ep_handle_create fail with EP_ERR_INVALID_ARG) at
+ * creation; ep_handle_set_topk_idx_bits changes it for later calls.  The
+ * pages list EP_NUM_TOPK_IDX_BITS as the variable that overrides the number
+ * of bits of the top-k index encoding (vi.news.hada.io, "Biến môi trường và
+ * giá trị cố định khi build").  int32 ids halve the bytes the routing reads.
+ * A `topk_idx` pointer must be 8-byte aligned for int64 ids, 4-byte for
+ * int32.  ep_get_dispatch_layout_noalloc always reads int64. */
+ep_status_t ep_handle_set_topk_idx_bits(ep_handle_t h, int bits);
+int ep_handle_topk_idx_bits(ep_handle_t h); /* 64 or 32; 0 for NULL */
+
 /* Free the handle's device and host memory.  The caller must make sure no
  * enqueued work that uses the handle is still pending.  NULL is a no-op. */
 ep_status_t ep_handle_destroy(ep_handle_t h);
 
 /* get_dispatch_layout ("DeepEP 要約" section 3, training forward;
  * devtrends.ru "Как это выглядит в коде", num_tokens_per_rank).
- * In:  topk_idx   dev int64 [T][k]; -1 marks a masked entry.
+ * In:  topk_idx   dev [T][k] ids, int64 or int32 (ep_handle_set_topk_idx_bits);
+ *                 -1 marks a masked entry.
  *      T          number of tokens, a multiple of R, <= R*max_tokens_per_rank.
  * Out (each may be NULL):
  *      num_tokens_per_rank    dev int32 [R src][R dst]: tokens source rank s
@@ -104,7 +118,7 @@ ep_status_t ep_handle_destroy(ep_handle_t h);
  * destination ranks and its row inside every destination rank's region
  * (rows ordered by source rank, then token), the regions' offsets inside the
  * packed receive buffer and the per-rank / per-expert receive counts. */
-ep_status_t ep_get_dispatch_layout(ep_handle_t h, const int64_t* topk_idx, int num_tokens,
+ep_status_t ep_get_dispatch_layout(ep_handle_t h, const void* topk_idx, int num_tokens,
                                    int* num_tokens_per_rank, int* num_tokens_per_expert,
                                    uint8_t* is_token_in_rank, ep_stream_t stream);
 
@@ -144,6 +158,27 @@ ep_status_t ep_dispatch(ep_handle_t h, const void* x, const float* topk_weights,
                         int* recv_src_idx, int* recv_topk_idx, float* recv_topk_weights,
                         int num_sms, ep_stream_t stream);
 
+/* get_dispatch_layout and dispatch in one call ("DeepEP 要約" section 3,
+ * training / prefill forward).  Same inputs and outputs as
+ * ep_get_dispatch_layout(topk_idx, T, NULL, NULL, NULL) followed by
+ * ep_dispatch(...), and the same handle state afterwards (so ep_combine,
+ * ep_get_num_recv and a cached-handle ep_dispatch work as usual); the
+ * per-source-rank counts and is_token_in_rank are not produced -- call
+ * ep_get_dispatch_layout when they are needed.
+ * Because the receive counts are only known on the device, recv_x must have
+ * room for the rows this routing produces (at most T * min(k, R)); rows past
+ * recv_capacity_rows latch EP_ERR_CAPACITY as in ep_dispatch.
+ * For R <= 64 and up to 4096 (token, k) entries per SM this is one
+ * cooperative launch: one block per SM ranks its own run of tokens while its
+ * rows are already streaming into shared memory, the blocks exchange counts
+ * through one grid barrier, then the rows are written.  Otherwise it runs the
+ * layout kernel and the dispatch kernel. */
+ep_status_t ep_layout_and_dispatch(ep_handle_t h, const void* topk_idx, int num_tokens, const void* x,
+                                   const float* topk_weights, ep_dtype_t dtype, void* recv_x,
+                                   float* recv_scales, int64_t recv_capacity_rows, int* recv_src_idx,
+                                   int* recv_topk_idx, float* recv_topk_weights, int num_sms,
+                                   ep_stream_t stream);
+
 /* combine, normal mode ("DeepEP 要約" section 3; vi.news.hada.io: combine
  * reduces the expert outputs back to the originating rank).
  * In:  y      dev bf16 [y_rows][H], laid out like dispatch's recv_x.
@@ -155,11 +190,37 @@ ep_status_t ep_dispatch(ep_handle_t h, const void* x, const float* topk_weights,
 ep_status_t ep_combine(ep_handle_t h, const void* y, int64_t y_rows, void* out, int num_sms,
                        ep_stream_t stream);
 
+/* combine, normal mode, general form.  ep_combine(h, y, rows, out, ...) is
+ * ep_combine_ex(h, EP_BF16, y, NULL, rows, NULL, out, NULL, ...).
+ * In:  y_dtype  EP_BF16: y is dev bf16 [y_rows][H];
+ *               EP_FP8_E4M3: y is dev e4m3 bytes [y_rows][H] with y_scales
+ *               dev fp32 [y_rows][H/128]; each value enters the sum as
+ *               e4m3 * scale (one fp32 multiply, nearest-even) -- a
+ *               low-precision combine input, as the pages' FP8 support
+ *               ("DeepSeek công bố thư viện mã nguồn mở DeepEP ...",
+ *               vi.news.hada.io: FP8 and other low precisions) extended to
+ *               the reduction side.
+ *      recv_topk_weights  dev fp32 [y_rows][k] or NULL, laid out like
+ *               dispatch's recv_topk_weights.
+ * Out: out      dev bf16 [T][H], the sum in ascending rank order as
+ *               ep_combine.
+ *      combined_topk_weights  dev fp32 [T][k], required exactly when
+ *               recv_topk_weights is given: column j of token t = the fp32
+ *               sum over t's rows, ascending rank, from +0.0, of
+ *               recv_topk_weights[row][j].  On dispatch's own output this
+ *               gives back topk_weights (0 where masked); on gradients it is
+ *               the backward of the weights ("DeepEP 要約" section 3: the
+ *               backward of dispatch is combine). */
+ep_status_t ep_combine_ex(ep_handle_t h, ep_dtype_t y_dtype, const void* y, const float* y_scales,
+                          int64_t y_rows, const float* recv_topk_weights, void* out,
+                          float* combined_topk_weights, int num_sms, ep_stream_t stream);
+
 /* low_latency_dispatch (devtrends.ru "Как это выглядит в коде";
  * "DeepEP 要約" section 3, decode).  Computes its own routing (no separate
  * layout call, no host synchronisation, capturable in a CUDA graph) and
  * stores it in the handle for ep_low_latency_combine.
- * In:  x         dev bf16 [T][H];  topk_idx dev int64 [T][k];  T as above.
+ * In:  x         dev bf16 [T][H];  topk_idx dev [T][k] (int64 or int32, as the
+ *                handle's setting);  T as above.
  * Out: recv_x       dev [E][M][H] (bf16 or e4m3), M = R * max_tokens_per_rank;
  *                   expert e = (rank e / E_l, local expert e % E_l); the
  *                   entries routed to e fill rows 0..count-1 in (source rank,
@@ -169,9 +230,11 @@ ep_status_t ep_combine(ep_handle_t h, const void* y, int64_t y_rows, void* out, 
  *      recv_count   dev int32 [E] or NULL: rows filled per expert.
  * Rows past M (only possible with duplicated ids in one token) are skipped
  * and latch EP_ERR_CAPACITY.
- * Two launches: a routing kernel (one block per chunk of 1024 (token, k)
- * entries) and the row scatter, which occupies at most num_sms SMs (0 = all). */
-ep_status_t ep_low_latency_dispatch(ep_handle_t h, const void* x, const int64_t* topk_idx,
+ * Usually one cooperative launch on at most num_sms SMs (0 = all): each
+ * block ranks its own run of tokens, the blocks exchange counts through one
+ * grid barrier, then the rows move.  With more than 4096 (token, k) entries
+ * per SM it is a routing kernel followed by the row scatter. */
+ep_status_t ep_low_latency_dispatch(ep_handle_t h, const void* x, const void* topk_idx,
                                     int num_tokens, ep_dtype_t dtype, void* recv_x,
                                     float* recv_scales, int* recv_src_info, int* recv_count,
                                     int num_sms, ep_stream_t stream);

@@ -161,3 +161,37 @@ def ll_path(R, E, k, H, idx, w, x, fp8, y_seed=None, num_sms=0, handle=None):
         frac = assert_bf16_close(host_bits(out), oracle.ll_combine(R, E, k, M, idx, w, y_host), "ll combine")
     assert h.get_device_status() == ep.EP_OK
     return h, ref, frac
+
+
+def fused_path(R, E, k, H, idx, w, x, fp8, y=None, num_sms=0, handle=None, cap=None):
+    """ep_layout_and_dispatch through the ABI: the handle's layout state
+    (counts, offsets, and -- through combine -- the destination rows) and the
+    dispatch outputs, each against the oracle."""
+    T = idx.shape[0]
+    h = handle or ep.Handle(R, E, k, H, max(T // R, 1))
+    L = oracle.layout(R, E, k, idx)
+    P = int(L["rank_offset"][-1])
+    cap = P if cap is None else cap
+    rows = max(cap, 1)
+    got = dict(
+        recv_x=torch.empty((rows, H), dtype=torch.uint8 if fp8 else torch.bfloat16, device=DEV)[:cap],
+        recv_scales=torch.empty((rows, H // 128), dtype=torch.float32, device=DEV)[:cap] if fp8 else None,
+        recv_src_idx=torch.full((rows,), -7, dtype=torch.int32, device=DEV)[:cap],
+        recv_topk_idx=torch.full((rows, k), -7, dtype=torch.int32, device=DEV)[:cap],
+        recv_topk_weights=torch.full((rows, k), -7.0, dtype=torch.float32, device=DEV)[:cap],
+    )
+    h.layout_and_dispatch(dev(idx), dev(x), dev(w), ep.EP_FP8_E4M3 if fp8 else ep.EP_BF16, got["recv_x"],
+                          got["recv_scales"], recv_src_idx=got["recv_src_idx"], recv_topk_idx=got["recv_topk_idx"],
+                          recv_topk_weights=got["recv_topk_weights"], num_sms=num_sms)
+    per_rank, per_expert, offset, st = h.get_num_recv()
+    assert np.array_equal(per_rank, L["num_recv_per_rank"]), "num_recv_tokens_per_rank"
+    assert np.array_equal(per_expert, L["num_recv_per_expert"]), "num_recv_tokens_per_expert"
+    assert np.array_equal(offset, L["rank_offset"]), "rank_offset"
+    ref, st = oracle.dispatch(R, E, k, x, idx, w, fp8=fp8)
+    compare_dispatch(got, ref, fp8, P)
+    frac = None
+    if y is not None:
+        comb = run_combine(h, y, num_sms=num_sms)
+        frac = assert_bf16_close(comb, oracle.combine(R, E, k, idx, y), "combine after fused dispatch")
+    assert h.get_device_status() == ep.EP_OK
+    return h, L, ref, frac

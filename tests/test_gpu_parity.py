@@ -12,7 +12,7 @@ import oracle
 from combine_ep_get_03_gb300 import ep
 from combine_ep_get_03_gb300 import workloads as wl
 
-from harness import (DEV, assert_bf16_close, check_layout, compare_dispatch, dev, host_bits, ll_path,
+from harness import (DEV, assert_bf16_close, check_layout, compare_dispatch, dev, fused_path, host_bits, ll_path,
                      normal_path, run_combine, run_dispatch)
 
 pytestmark = pytest.mark.gpu
@@ -138,6 +138,61 @@ def test_long_scatter_pipelines(H):
         normal_path(R, E, k, H, idx, w, x, fp8=fp8, y=y, handle=h)
         normal_path(R, E, k, H, idx, w, x, fp8=fp8, handle=h, num_sms=7)
         ll_path(R, E, k, H, idx, w, x, fp8=fp8, y_seed=3, handle=h)
+    h.close()
+
+
+# ------------------------------------------------------------ fused layout + dispatch
+
+@pytest.mark.parametrize("name", ["tiny_bf16", "v3_ep8", "v3_ep8_group_limited", "large_ep64_bwd"])
+def test_fused_layout_dispatch_workloads(name):
+    w_ = wl.WORKLOADS[name]
+    x, idx, wts = wl.make_inputs(w_)
+    P = int(oracle.layout(w_.R, w_.E, w_.k, idx)["rank_offset"][-1])
+    y = wl.expert_outputs(w_, P)
+    h, _, _, frac = fused_path(w_.R, w_.E, w_.k, w_.H, idx, wts, x, fp8=w_.fp8, y=y)
+    assert frac == 1.0
+    # the handle serves a cached-handle (backward) dispatch afterwards
+    g = wl.normal_bf16(wl.rng(w_.seed + 200), (w_.T, w_.H), 1e-2)
+    got = run_dispatch(h, dev(g), dev(wts), False, P)
+    ref, _ = oracle.dispatch(w_.R, w_.E, w_.k, g, idx, wts, fp8=False)
+    compare_dispatch(got, ref, False, P)
+    h.close()
+
+
+@pytest.mark.parametrize("case", EDGE, ids=[f"R{c[0]}E{c[1]}k{c[2]}H{c[3]}t{c[4]}" for c in EDGE])
+def test_fused_layout_dispatch_edge_shapes(case):
+    R, E, k, H, tpr, mask, dup = case
+    idx, w, x = _edge_inputs(R, E, k, H, tpr, mask, dup, seed=sum(case[:5]) + 1)
+    y = wl.normal_bf16(wl.rng(3), (int(oracle.layout(R, E, k, idx)["rank_offset"][-1]), H))
+    h = ep.Handle(R, E, k, H, tpr)
+    for fp8 in (False, True):
+        fused_path(R, E, k, H, idx, w, x, fp8=fp8, y=y, handle=h)
+    h.close()
+
+
+@pytest.mark.parametrize("num_sms", [1, 7])
+def test_fused_on_few_sms(num_sms):
+    """One block (the grid barrier degenerates) and a handful of blocks."""
+    R, E, k, H, tpr = 8, 64, 8, 1024, 48
+    idx, w, x = _edge_inputs(R, E, k, H, tpr, 0.02, 0.1, seed=60 + num_sms)
+    y = wl.normal_bf16(wl.rng(61), (int(oracle.layout(R, E, k, idx)["rank_offset"][-1]), H))
+    h = ep.Handle(R, E, k, H, tpr)
+    fused_path(R, E, k, H, idx, w, x, fp8=True, y=y, handle=h, num_sms=num_sms)
+    ll_path(R, E, k, H, idx, w, x, fp8=True, y_seed=62, handle=h, num_sms=num_sms)
+    h.close()
+
+
+@pytest.mark.parametrize("case", [(128, 128, 4, 128, 2), (8, 64, 8, 128, 10240)],
+                         ids=["R128_layout_kernel", "T81920_routing_kernels"])
+def test_fused_falls_back_to_separate_kernels(case):
+    """More ranks than a 64-bit mask holds, or more than 4096 (token, k)
+    entries per SM: the same results through the separate kernels."""
+    R, E, k, H, tpr = case
+    idx, w, x = _edge_inputs(R, E, k, H, tpr, 0.02, 0.0, seed=sum(case))
+    y = wl.normal_bf16(wl.rng(70), (int(oracle.layout(R, E, k, idx)["rank_offset"][-1]), H))
+    h = ep.Handle(R, E, k, H, tpr)
+    fused_path(R, E, k, H, idx, w, x, fp8=True, y=y, handle=h)
+    ll_path(R, E, k, H, idx, w, x, fp8=True, y_seed=71, handle=h)
     h.close()
 
 

@@ -1,0 +1,186 @@
+"""GPU parity for the general combine (e4m3 input, the top-k weights'
+reduction) and for int32 top-k ids, through the C ABI, against the oracle.
+
+Bars: e4m3 combine output within 1 bf16 ulp and >= 99.9% bit-exact (both
+sides take decode * scale as one fp32 multiply and add in ascending rank
+order, so 100% is expected); combined top-k weights bit-exact; everything
+routed from int32 ids bit-identical to the int64 run's oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_ep_get_03_gb300 import ep
+from combine_ep_get_03_gb300 import workloads as wl
+from harness import DEV, assert_bf16_close, dev, fused_path, host_bits, ll_path, normal_path, run_dispatch
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(R, E, k, H, tpr, seed, mask=0.02, dup=0.0):
+    g = wl.rng(seed)
+    T = R * tpr
+    idx, w = wl.route_uniform(g, T, E, k)
+    idx = wl.mask_entries(g, idx, mask)
+    if dup:
+        sel = g.random(T) < dup
+        idx[sel, k - 1] = idx[sel, 0]
+    x = wl.normal_bf16(g, (T, H))
+    return idx, w, x
+
+
+CASES = [(4, 16, 2, 256, 16), (8, 64, 8, 1024, 64), (8, 256, 8, 7168, 96), (64, 256, 8, 512, 8), (3, 12, 4, 384, 33)]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"R{c[0]}E{c[1]}k{c[2]}H{c[3]}t{c[4]}" for c in CASES])
+def test_combine_fp8_input_and_weights(case):
+    R, E, k, H, tpr = case
+    idx, w, x = _inputs(R, E, k, H, tpr, seed=sum(case))
+    h, L, ref, _ = normal_path(R, E, k, H, idx, w, x, fp8=True)
+    P = int(L["rank_offset"][-1])
+    T = idx.shape[0]
+    # e4m3 expert outputs: the dispatched rows themselves, then random codes
+    # and scales (NaN codes excluded)
+    g = wl.rng(7 + R)
+    q_rand = g.integers(0, 256, (P, H), dtype=np.uint8)
+    q_rand[(q_rand & 0x7F) == 0x7F] = 0
+    s_rand = (g.random((P, H // 128)) * 3 + 1e-3).astype(np.float32)
+    rw = (g.random((P, k)) - 0.5).astype(np.float32)
+    for q, s in ((ref["recv_x"][:P], ref["recv_scales"][:P]), (q_rand, s_rand)):
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+        cw = torch.full((T, k), -7.0, dtype=torch.float32, device=DEV)
+        h.combine_ex(dev(q), out, y_scales=dev(s), recv_topk_weights=dev(rw), combined_topk_weights=cw)
+        ref_out, ref_cw = oracle.combine_ex(R, E, k, idx, q, y_scales=s, recv_topk_weights=rw)
+        frac = assert_bf16_close(host_bits(out), ref_out, "e4m3 combine")
+        assert frac == 1.0
+        assert np.array_equal(cw.cpu().numpy().view(np.uint32), ref_cw.view(np.uint32)), "combined_topk_weights"
+    # bf16 y through the general entry point equals the plain combine
+    y = wl.normal_bf16(g, (P, H))
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    h.combine_ex(dev(y), out)
+    assert np.array_equal(host_bits(out), oracle.combine(R, E, k, idx, y))
+    assert h.get_device_status() == ep.EP_OK
+    h.close()
+
+
+def test_combined_weights_undo_dispatch():
+    """combine(recv_topk_weights of a dispatch) gives back the weights."""
+    R, E, k, H, tpr = 8, 64, 8, 256, 40
+    idx, w, x = _inputs(R, E, k, H, tpr, seed=90, dup=0.2)
+    h, L, ref, _ = normal_path(R, E, k, H, idx, w, x, fp8=False)
+    P = int(L["rank_offset"][-1])
+    T = idx.shape[0]
+    got = run_dispatch(h, dev(x), dev(w), False, P)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    cw = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    h.combine_ex(got["recv_x"], out, recv_topk_weights=got["recv_topk_weights"], combined_topk_weights=cw)
+    assert np.array_equal(cw.cpu().numpy(), np.where(idx >= 0, w, np.float32(0)))
+    h.close()
+
+
+def test_combine_ex_argument_errors():
+    R, E, k, H, tpr = 4, 16, 2, 256, 8
+    idx, w, x = _inputs(R, E, k, H, tpr, seed=91)
+    h, L, _, _ = normal_path(R, E, k, H, idx, w, x, fp8=False)
+    P = int(L["rank_offset"][-1])
+    T = idx.shape[0]
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    y8 = torch.zeros((P, H), dtype=torch.uint8, device=DEV)
+    rw = torch.zeros((P, k), dtype=torch.float32, device=DEV)
+    L_ = ep.lib()
+    # e4m3 rows without scales; weights in without weights out
+    assert L_.ep_combine_ex(h.ptr, ep.EP_FP8_E4M3, y8.data_ptr(), None, P, None, out.data_ptr(), None, 0,
+                            None) == ep.EP_ERR_INVALID_ARG
+    assert L_.ep_combine_ex(h.ptr, ep.EP_BF16, y8.data_ptr(), None, P, rw.data_ptr(), out.data_ptr(), None, 0,
+                            None) == ep.EP_ERR_INVALID_ARG
+    assert L_.ep_combine_ex(h.ptr, 7, y8.data_ptr(), None, P, None, out.data_ptr(), None, 0,
+                            None) == ep.EP_ERR_INVALID_ARG
+    h.close()
+
+
+# ------------------------------------------------------------ int32 top-k ids
+
+def _handle32(R, E, k, H, tpr):
+    h = ep.Handle(R, E, k, H, tpr)
+    h.set_topk_idx_bits(32)
+    assert h.topk_idx_bits == 32
+    return h
+
+
+@pytest.mark.parametrize("case", CASES[:4], ids=[f"R{c[0]}E{c[1]}k{c[2]}H{c[3]}t{c[4]}" for c in CASES[:4]])
+def test_int32_ids_every_routing_path(case):
+    R, E, k, H, tpr = case
+    idx, w, x = _inputs(R, E, k, H, tpr, seed=sum(case) + 5, dup=0.1)
+    idx32 = idx.astype(np.int32)
+    T = idx.shape[0]
+    h = _handle32(R, E, k, H, tpr)
+    # layout, then dispatch and combine on it
+    L = oracle.layout(R, E, k, idx)
+    ntpr = torch.full((R, R), -9, dtype=torch.int32, device=DEV)
+    ntpe = torch.full((R, E), -9, dtype=torch.int32, device=DEV)
+    itr = torch.zeros((T, R), dtype=torch.bool, device=DEV)
+    h.get_dispatch_layout(dev(idx32), num_tokens_per_rank=ntpr, num_tokens_per_expert=ntpe, is_token_in_rank=itr)
+    per_rank, per_expert, offset, _ = h.get_num_recv()
+    assert np.array_equal(ntpr.cpu().numpy(), L["num_tokens_per_rank"])
+    assert np.array_equal(ntpe.cpu().numpy(), L["num_tokens_per_expert"])
+    assert np.array_equal(itr.cpu().numpy(), L["is_token_in_rank"])
+    assert np.array_equal(offset, L["rank_offset"]) and np.array_equal(per_expert, L["num_recv_per_expert"])
+    P = int(L["rank_offset"][-1])
+    got = run_dispatch(h, dev(x), dev(w), True, P)
+    ref, _ = oracle.dispatch(R, E, k, x, idx, w, fp8=True)
+    assert np.array_equal(got["recv_x"].cpu().numpy(), ref["recv_x"][:P])
+    assert np.array_equal(got["recv_topk_idx"].cpu().numpy(), ref["recv_topk_idx"][:P])
+    # fused layout + dispatch
+    recv = torch.empty((max(P, 1), H), dtype=torch.uint8, device=DEV)[:P]
+    sc = torch.empty((max(P, 1), H // 128), dtype=torch.float32, device=DEV)[:P]
+    src = torch.full((max(P, 1),), -7, dtype=torch.int32, device=DEV)[:P]
+    h.layout_and_dispatch(dev(idx32), dev(x), dev(w), ep.EP_FP8_E4M3, recv, sc, recv_src_idx=src)
+    assert np.array_equal(recv.cpu().numpy(), ref["recv_x"][:P])
+    assert np.array_equal(src.cpu().numpy(), ref["recv_src_idx"][:P])
+    # low latency
+    M = h.M
+    ll = torch.empty((E, M, H), dtype=torch.bfloat16, device=DEV)
+    cnt = torch.full((E,), -7, dtype=torch.int32, device=DEV)
+    info = torch.full((E, M), -7, dtype=torch.int32, device=DEV)
+    h.low_latency_dispatch(dev(x), dev(idx32), ep.EP_BF16, ll, recv_src_info=info, recv_count=cnt)
+    lref, _ = oracle.ll_dispatch(R, E, k, M, x, idx, fp8=False)
+    count = cnt.cpu().numpy()
+    assert np.array_equal(count, lref["recv_count"])
+    for e in range(E):
+        assert np.array_equal(info[e, :count[e]].cpu().numpy(), lref["recv_src_info"][e, :count[e]])
+    assert h.get_device_status() == ep.EP_OK
+    h.close()
+
+
+def test_int32_ids_bad_id_latched_and_width_checked():
+    R, E, k, H, tpr = 4, 16, 2, 128, 8
+    idx, w, x = _inputs(R, E, k, H, tpr, seed=17)
+    idx32 = idx.astype(np.int32)
+    idx32[3, 1] = E   # out of range
+    h = _handle32(R, E, k, H, tpr)
+    h.get_dispatch_layout(dev(idx32))
+    assert h.get_device_status() == ep.EP_ERR_BAD_EXPERT
+    # an int64 table on an int32 handle is refused before any launch
+    with pytest.raises(ValueError):
+        h.get_dispatch_layout(dev(idx))
+    h.set_topk_idx_bits(64)
+    idx[3, 1] = 1
+    _, L, _, _ = normal_path(R, E, k, H, idx, w, x, fp8=False, handle=h)
+    with pytest.raises(ep.EPError):
+        h.set_topk_idx_bits(16)
+    h.close()
+
+
+def test_int32_ids_from_environment(monkeypatch):
+    monkeypatch.setenv("EP_NUM_TOPK_IDX_BITS", "32")
+    h = ep.Handle(4, 16, 2, 128, 8)
+    assert h.topk_idx_bits == 32
+    h.close()
+    monkeypatch.setenv("EP_NUM_TOPK_IDX_BITS", "12")
+    with pytest.raises(ep.EPError):
+        ep.Handle(4, 16, 2, 128, 8)
+    monkeypatch.delenv("EP_NUM_TOPK_IDX_BITS")
+    h = ep.Handle(4, 16, 2, 128, 8)
+    assert h.topk_idx_bits == 64
+    h.close()
