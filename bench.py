@@ -174,6 +174,98 @@ class Step:
         ]
 
 
+class NextOps:
+    """The calls beyond the step: the same batch routed from int32 ids, the
+    expert-major layout (groups aligned to 128 rows) with its combine, and
+    the general combine (e4m3 input; the top-k weights' reduction).  Each is
+    timed on its own with events, like the step's ops."""
+
+    ALIGN = 128
+
+    def __init__(self, step: Step):
+        w, dev = step.w, step.dev
+        T, H, k, E = w.T, w.H, w.k, w.E
+        G = H // 128
+        self.step = step
+        self.h32 = ep.Handle(w.R, E, k, H, w.tokens_per_rank)
+        self.h32.set_topk_idx_bits(32)
+        self.idx32 = step.idx.to(torch.int32)
+        rows_cap, _ = ep.ep_get_buffer_size_hint(w.R, E, k, H, w.tokens_per_rank, ep.EP_FP8_E4M3,
+                                                 ep.EP_LAYOUT_EXPERT_MAJOR, self.ALIGN)
+        self.em_recv = torch.empty((rows_cap, H), dtype=torch.uint8, device=dev)
+        self.em_scales = torch.empty((G, (rows_cap + 3) // 4 * 4), dtype=torch.float32, device=dev)
+        self.em_src = torch.empty(rows_cap, dtype=torch.int32, device=dev)
+        self.em_w = torch.empty(rows_cap, dtype=torch.float32, device=dev)
+        self.em_call()
+        counts, offsets, _ = step.h.em_get_layout()
+        self.n_em, self.rows_em = int(counts.sum()), int(offsets[-1])
+        gen = torch.Generator(device=dev).manual_seed(w.seed * 7907)
+        self.y_em = (torch.randn((self.rows_em, H), generator=gen, device=dev) * w.y_sigma).to(torch.bfloat16)
+        self.out_em = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        self.cw = torch.empty((T, k), dtype=torch.float32, device=dev)
+        self.out8 = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        self.recv32 = torch.empty_like(step.recv)
+        self.scales32 = torch.empty_like(step.scales)
+        P = step.sizes.P
+        row8 = H + 4 * G
+        dst = 8 * T * min(k, w.R)
+        self.hbm = {
+            "layout_dispatch_fp8_ids32": step.sizes.hbm["layout_dispatch_fp8"] - 4 * T * k,
+            "em_layout_dispatch_fp8": 8 * T * k + 8 * T * k + 2 * T * H + 4 * T * k
+                                      + self.n_em * (H + 4 * G + 8) + 8 * (self.rows_em - self.n_em),
+            "em_combine": self.n_em * 2 * H + 2 * T * H + 8 * T * k,
+            "combine_fp8_input": P * row8 + 2 * T * H + dst,
+            "combine_with_weights": P * 2 * H + P * 4 * k + 2 * T * H + 4 * T * k + dst,
+        }
+        self.logical = {
+            "layout_dispatch_fp8_ids32": P * row8,
+            "em_layout_dispatch_fp8": self.n_em * row8,
+            "em_combine": self.n_em * 2 * H,
+            "combine_fp8_input": P * row8,
+            "combine_with_weights": P * 2 * H,
+        }
+        torch.cuda.synchronize(dev)
+
+    def em_call(self):
+        s = self.step
+        s.h.em_layout_and_dispatch(s.idx, s.x, s.wts, ep.EP_FP8_E4M3, self.ALIGN, self.em_recv, self.em_scales,
+                                   recv_src_idx=self.em_src, recv_weights=self.em_w, num_sms=s.num_sms)
+
+    def ops(self):
+        s, n = self.step, self.step.num_sms
+        return [
+            ("layout_dispatch_fp8_ids32", lambda: self.h32.layout_and_dispatch(
+                self.idx32, s.x, s.wts, ep.EP_FP8_E4M3, self.recv32, self.scales32, num_sms=n)),
+            ("em_layout_dispatch_fp8", self.em_call),
+            ("em_combine", lambda: s.h.em_combine(self.y_em, self.out_em, num_sms=n)),
+            ("combine_fp8_input", lambda: s.h.combine_ex(s.recv, self.out8, y_scales=s.scales, num_sms=n)),
+            ("combine_with_weights", lambda: s.h.combine_ex(s.y, s.out, recv_topk_weights=s.rw,
+                                                            combined_topk_weights=self.cw, num_sms=n)),
+        ]
+
+    def time(self, K: int, stream: torch.cuda.Stream, peak: float):
+        ops = self.ops()
+        for _, fn in ops:
+            fn()
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(K)]
+        for r in range(K):
+            ev[r][0].record(stream)
+            for i, (_, fn) in enumerate(ops):
+                fn()
+                ev[r][i + 1].record(stream)
+        ev[-1][-1].synchronize()
+        res = {}
+        for i, (name, _) in enumerate(ops):
+            ts = [ev[r][i].elapsed_time(ev[r][i + 1]) for r in range(K)]
+            ms = statistics.fmean(ts)
+            res[name] = {"us": round(ms * 1e3, 2), "logical_gbs": round(self.logical[name] / (ms / 1e3) / 1e9, 1),
+                         "hbm_gbs": round(self.hbm[name] / (ms / 1e3) / 1e9, 1),
+                         "hbm_frac": round(self.hbm[name] / (ms / 1e3) / 1e9 / peak, 4)}
+        res["em_rows"] = {"entries": self.n_em, "rows_with_padding": self.rows_em, "alignment": self.ALIGN}
+        return res
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during a region."""
 
@@ -569,6 +661,11 @@ def main():
         "gpu_launches": len(OPS) * args.steps,
         "clocks": clocks,
     }
+    nxt = NextOps(step)
+    line["next_ops"] = nxt.time(min(args.steps, 100), stream, peak)
+    status = step.h.get_device_status()
+    if status != ep.EP_OK:
+        raise RuntimeError(f"device status after the next-row ops: {ep.status_str(status)}")
     line["ll_decode"] = ll_decode_latency(dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # whole-batch oracle steps until about 10 s of CPU work (at most 3)

@@ -1,6 +1,7 @@
 // The C ABI declared in include/ep.h: handle lifecycle, argument checks,
 // launch configuration and the device status latch.  Every step of the
 // computation runs in this library's kernels; there is no host fallback.
+#include <climits>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -22,13 +23,14 @@ struct ep_handle {
   // occupancy (blocks per SM) of the persistent kernels
   int occ_dispatch[2], occ_combine[4];  // combine: rank-major bf16, rank-major e4m3, low latency, expert-major
   // TMA scatter: row stages and consumer warps per block for
-  // [fp8][low_latency]; 0 stages = rows too long, the register-resident
-  // kernels are used instead
-  int scatter_ns[2][2], scatter_nc[2][2];
+  // [fp8][rank-major, low latency, expert-major]; 0 stages = rows too long,
+  // the register-resident kernels are used instead (none for expert-major)
+  int scatter_ns[2][3], scatter_nc[2][3];
   size_t ll_route_smem;
   // state
   int T_layout;  // tokens of the last layout, -1 before the first
   int T_ll;      // tokens of the last low-latency dispatch, -1 before the first
+  int T_em;      // tokens of the last expert-major layout, -1 before the first
   bool debug;
   // device arena
   void* arena;
@@ -41,7 +43,14 @@ struct ep_handle {
   int* ll_slot;
   unsigned long long* layout_flags;
   unsigned long long* ll_flags;
-  unsigned long long* tickets;  // [0] layout, [1] low latency: (epoch << 32) | next chunk id
+  unsigned long long* em_flags;
+  unsigned long long* tickets;  // [0] layout, [1] low latency, [2] expert-major: (epoch << 32) | next chunk id
+  // expert-major layout: per entry expert id and slot inside the expert,
+  // per expert count and group offset
+  int* em_idx;
+  int* em_slot;
+  int* em_count;
+  int* em_offset;
   int* fused_agg;               // [num_sms][R+E] per-block counts of the fused kernel
   unsigned* fused_barrier;      // [2] its grid barrier words
   size_t smem_optin;
@@ -183,6 +192,7 @@ ep_status_t ep_handle_create(int R, int E, int k, int H, int max_tpr, ep_handle_
   }
   h->T_layout = -1;
   h->T_ll = -1;
+  h->T_em = -1;
   h->debug = std::getenv("EP_DEBUG") != nullptr;
 
   ep_status_t st = EP_OK;
@@ -230,7 +240,12 @@ ep_status_t ep_handle_create(int R, int E, int k, int H, int max_tpr, ep_handle_
   const size_t o_llslot = take(sizeof(int) * static_cast<size_t>(h->Tmax) * k);
   const size_t o_lf = take(sizeof(unsigned long long) * static_cast<size_t>(h->layout_cmax) * NKl);
   const size_t o_llf = take(sizeof(unsigned long long) * static_cast<size_t>(h->ll_cmax) * NKll);
-  const size_t o_tk = take(sizeof(unsigned long long) * 2);
+  const size_t o_emf = take(sizeof(unsigned long long) * static_cast<size_t>(h->ll_cmax) * NKll);
+  const size_t o_tk = take(sizeof(unsigned long long) * 3);
+  const size_t o_emidx = take(sizeof(int) * static_cast<size_t>(h->Tmax) * k);
+  const size_t o_emslot = take(sizeof(int) * static_cast<size_t>(h->Tmax) * k);
+  const size_t o_emcnt = take(sizeof(int) * E);
+  const size_t o_emoff = take(sizeof(int) * (E + 1));
   const size_t o_fagg = take(sizeof(int) * static_cast<size_t>(h->num_sms) * (R + E));
   const size_t o_fbar = take(sizeof(unsigned) * 2);
   const size_t o_err = take(sizeof(int));
@@ -248,17 +263,22 @@ ep_status_t ep_handle_create(int R, int E, int k, int H, int max_tpr, ep_handle_
   h->ll_slot = reinterpret_cast<int*>(base + o_llslot);
   h->layout_flags = reinterpret_cast<unsigned long long*>(base + o_lf);
   h->ll_flags = reinterpret_cast<unsigned long long*>(base + o_llf);
+  h->em_flags = reinterpret_cast<unsigned long long*>(base + o_emf);
   h->tickets = reinterpret_cast<unsigned long long*>(base + o_tk);
+  h->em_idx = reinterpret_cast<int*>(base + o_emidx);
+  h->em_slot = reinterpret_cast<int*>(base + o_emslot);
+  h->em_count = reinterpret_cast<int*>(base + o_emcnt);
+  h->em_offset = reinterpret_cast<int*>(base + o_emoff);
   h->fused_agg = reinterpret_cast<int*>(base + o_fagg);
   h->fused_barrier = reinterpret_cast<unsigned*>(base + o_fbar);
   h->err = reinterpret_cast<int*>(base + o_err);
   // zero everything once (latch, look-back words); tickets start at epoch 1,
   // so no look-back word ever matches before it is written
-  const unsigned long long first_ticket[2] = {1ull << 32, 1ull << 32};
+  const unsigned long long first_ticket[3] = {1ull << 32, 1ull << 32, 1ull << 32};
   if ((st = cuda_status(cudaMemset(h->arena, 0, off), "cudaMemset")) != EP_OK ||
       (st = cuda_status(cudaMemcpy(h->tickets, first_ticket, sizeof(first_ticket), cudaMemcpyHostToDevice),
                         "cudaMemcpy")) != EP_OK ||
-      (st = cuda_status(cudaMallocHost(&h->host, sizeof(int) * (1 + 2 * R + E + 1)), "cudaMallocHost")) != EP_OK) {
+      (st = cuda_status(cudaMallocHost(&h->host, sizeof(int) * (2 + 2 * R + 2 * E + 2)), "cudaMallocHost")) != EP_OK) {
     cudaFree(h->arena);
     delete h;
     return st;
@@ -269,7 +289,7 @@ ep_status_t ep_handle_create(int R, int E, int k, int H, int max_tpr, ep_handle_
   const size_t optin = static_cast<size_t>(prop.sharedMemPerBlockOptin);
   h->smem_optin = optin;
   for (int f = 0; f < 2; ++f)
-    for (int l = 0; l < 2; ++l) ep::scatter_config(H, R, f == 1, l == 1, optin, &h->scatter_ns[f][l], &h->scatter_nc[f][l]);
+    for (int m = 0; m < 3; ++m) ep::scatter_config(H, R, E, f == 1, m, optin, &h->scatter_ns[f][m], &h->scatter_nc[f][m]);
   if ((st = cuda_status(ep::configure_layout(h->layout_smem), "configure_layout")) != EP_OK ||
       (st = cuda_status(ep::configure_ll_dispatch(h->ll_smem), "configure_ll_dispatch")) != EP_OK ||
       (st = cuda_status(ep::configure_ll_route(h->ll_route_smem), "configure_ll_route")) != EP_OK ||
@@ -393,7 +413,7 @@ ep_status_t ep_dispatch(ep_handle_t h, const void* x, const float* topk_weights,
   ep_status_t st = check_device(h);
   if (st != EP_OK) return st;
   if (T == 0) return EP_OK;
-  const int sns = h->scatter_ns[fp8 ? 1 : 0][0], snc = h->scatter_nc[fp8 ? 1 : 0][0];
+  const int sns = h->scatter_ns[fp8 ? 1 : 0][ep::kSrcRanks], snc = h->scatter_nc[fp8 ? 1 : 0][ep::kSrcRanks];
   if (sns > 0) {
     ep::ScatterArgs a{};
     a.x = static_cast<const uint16_t*>(x);
@@ -403,6 +423,7 @@ ep_status_t ep_dispatch(ep_handle_t h, const void* x, const float* topk_weights,
     a.kmax = h->kmax;
     a.El = h->El;
     a.R = h->R;
+    a.E = h->E;
     a.dst = h->dst;
     a.rank_offset = h->rank_offset;
     a.cap = cap;
@@ -415,7 +436,7 @@ ep_status_t ep_dispatch(ep_handle_t h, const void* x, const float* topk_weights,
     a.recv_scales = recv_scales;
     a.err = h->err;
     const int blocks = grid_for(h, 1, num_sms, T, 1);
-    ep::launch_scatter(a, fp8, false, blocks, sns, snc, reinterpret_cast<cudaStream_t>(stream));
+    ep::launch_scatter(a, fp8, ep::kSrcRanks, blocks, sns, snc, reinterpret_cast<cudaStream_t>(stream));
     if (h->debug)
       std::fprintf(stderr, "[ep] dispatch %s T=%d: TMA scatter %d blocks, %d stages, %d consumers\n",
                    fp8 ? "fp8" : "bf16", T, blocks, sns, snc);
@@ -465,8 +486,8 @@ ep_status_t ep_layout_and_dispatch(ep_handle_t h, const void* topk_idx, int T, c
   if (st != EP_OK) return st;
   int fblocks = 0, fns = 0, fnc = 0;
   if (static_cast<long long>(T) * h->kmax < (1LL << 31))
-    ep::fused_config(false, fp8, T, h->R, h->E, h->k, h->kmax, h->H, sms_for(h, num_sms), h->smem_optin, &fblocks,
-                     &fns, &fnc);
+    ep::fused_config(ep::kSrcRanks, fp8, T, h->R, h->E, h->k, h->kmax, h->H, sms_for(h, num_sms), h->smem_optin,
+                     &fblocks, &fns, &fnc);
   if (fblocks == 0) {
     // the general path: layout kernel, then the scatter
     if ((st = ep_get_dispatch_layout(h, topk_idx, T, nullptr, nullptr, nullptr, stream)) != EP_OK) return st;
@@ -486,7 +507,7 @@ ep_status_t ep_layout_and_dispatch(ep_handle_t h, const void* topk_idx, int T, c
   f.recv_topk_weights = recv_topk_weights;
   f.recv_x = recv_x;
   f.recv_scales = recv_scales;
-  if ((st = cuda_status(ep::launch_fused(f, fp8, false, fblocks, fns, fnc, reinterpret_cast<cudaStream_t>(stream)),
+  if ((st = cuda_status(ep::launch_fused(f, fp8, ep::kSrcRanks, fblocks, fns, fnc, reinterpret_cast<cudaStream_t>(stream)),
                         "k_route_scatter launch")) != EP_OK)
     return st;
   if (h->debug)
@@ -561,8 +582,8 @@ ep_status_t ep_low_latency_dispatch(ep_handle_t h, const void* x, const void* to
     return EP_OK;
   }
   int fblocks = 0, fns = 0, fnc = 0;
-  ep::fused_config(true, fp8, T, h->R, h->E, h->k, h->kmax, h->H, sms_for(h, num_sms), h->smem_optin, &fblocks,
-                   &fns, &fnc);
+  ep::fused_config(ep::kSrcLowLatency, fp8, T, h->R, h->E, h->k, h->kmax, h->H, sms_for(h, num_sms), h->smem_optin,
+                   &fblocks, &fns, &fnc);
   if (fblocks > 0) {
     // routing and row movement in one cooperative launch
     ep::FusedArgs f = fused_args(h, topk_idx, static_cast<const uint16_t*>(x), nullptr, T);
@@ -574,7 +595,7 @@ ep_status_t ep_low_latency_dispatch(ep_handle_t h, const void* x, const void* to
     f.recv_src_info = recv_src_info;
     f.recv_x = recv_x;
     f.recv_scales = recv_scales;
-    if ((st = cuda_status(ep::launch_fused(f, fp8, true, fblocks, fns, fnc, s), "k_route_scatter(ll) launch")) !=
+    if ((st = cuda_status(ep::launch_fused(f, fp8, ep::kSrcLowLatency, fblocks, fns, fnc, s), "k_route_scatter(ll) launch")) !=
         EP_OK)
       return st;
     if (h->debug)
@@ -582,7 +603,7 @@ ep_status_t ep_low_latency_dispatch(ep_handle_t h, const void* x, const void* to
     h->T_ll = T;
     return EP_OK;
   }
-  const int sns = h->scatter_ns[fp8 ? 1 : 0][1], snc = h->scatter_nc[fp8 ? 1 : 0][1];
+  const int sns = h->scatter_ns[fp8 ? 1 : 0][ep::kSrcLowLatency], snc = h->scatter_nc[fp8 ? 1 : 0][ep::kSrcLowLatency];
   if (sns > 0) {
     // routing (slots, counts) on layout-sized chunks, then the TMA scatter
     RouteParams p = route_params(h, topk_idx, T, h->layout_CT, h->ll_flags, h->tickets + 1);
@@ -597,6 +618,7 @@ ep_status_t ep_low_latency_dispatch(ep_handle_t h, const void* x, const void* to
     a.kmax = h->kmax;
     a.El = h->El;
     a.R = h->R;
+    a.E = h->E;
     a.ll_idx = h->ll_idx;
     a.ll_slot = h->ll_slot;
     a.M = M;
@@ -605,7 +627,7 @@ ep_status_t ep_low_latency_dispatch(ep_handle_t h, const void* x, const void* to
     a.recv_scales = recv_scales;
     a.err = h->err;
     const int blocks = grid_for(h, 1, num_sms, T, 1);
-    ep::launch_scatter(a, fp8, true, blocks, sns, snc, s);
+    ep::launch_scatter(a, fp8, ep::kSrcLowLatency, blocks, sns, snc, s);
     if ((st = cuda_status(cudaGetLastError(), "k_scatter(ll) launch")) != EP_OK) return st;
     if (h->debug)
       std::fprintf(stderr, "[ep] ll dispatch T=%d: route %d blocks, TMA scatter %d blocks, %d stages, %d consumers\n",
@@ -661,6 +683,225 @@ ep_status_t ep_low_latency_combine(ep_handle_t h, const void* y, const float* to
   ep::launch_combine(a, ep::kSrcLowLatency, false, blocks, reinterpret_cast<cudaStream_t>(stream));
   if (h->debug) std::fprintf(stderr, "[ep] ll combine T=%d: %d blocks\n", T, blocks);
   return cuda_status(cudaGetLastError(), "k_combine(ll) launch");
+}
+
+// ---------------------------------------------------------------- expert-major
+
+namespace {
+
+ep_status_t em_check_outputs(const ep_handle* h, ep_dtype_t dtype, const float* topk_weights, void* recv_x,
+                             float* recv_scales, int64_t scales_ld, int64_t cap, int* recv_src_idx,
+                             float* recv_weights) {
+  if (dtype != EP_BF16 && dtype != EP_FP8_E4M3) return EP_ERR_INVALID_ARG;
+  const bool fp8 = dtype == EP_FP8_E4M3;
+  if (cap < 0 || cap > (1LL << 31) - 1 || (cap > 0 && !recv_x)) return EP_ERR_INVALID_ARG;
+  if (fp8 && cap > 0 && (!recv_scales || scales_ld < cap || scales_ld % 4 != 0)) return EP_ERR_INVALID_ARG;
+  if (recv_weights && !topk_weights) return EP_ERR_INVALID_ARG;
+  if ((recv_x && !aligned16(recv_x)) || (fp8 && recv_scales && !aligned16(recv_scales)) ||
+      (topk_weights && !aligned4(topk_weights)) || (recv_src_idx && !aligned4(recv_src_idx)) ||
+      (recv_weights && !aligned4(recv_weights)))
+    return EP_ERR_INVALID_ARG;
+  if (h->scatter_ns[fp8 ? 1 : 0][ep::kSrcExpertMajor] == 0) return EP_ERR_INVALID_ARG;  // rows too long to stage
+  return EP_OK;
+}
+
+// The rows of the handle's expert-major layout through the TMA scatter.
+ep_status_t em_scatter(ep_handle* h, const void* x, const float* topk_weights, bool fp8, void* recv_x,
+                       float* recv_scales, int64_t scales_ld, int64_t cap, int* recv_src_idx, float* recv_weights,
+                       int num_sms, cudaStream_t s) {
+  const int T = h->T_em;
+  ep::ScatterArgs a{};
+  a.x = static_cast<const uint16_t*>(x);
+  a.T = T;
+  a.H = h->H;
+  a.k = h->k;
+  a.kmax = h->kmax;
+  a.El = h->El;
+  a.R = h->R;
+  a.E = h->E;
+  a.cap = cap;
+  a.topk_weights = topk_weights;
+  a.ll_idx = h->em_idx;
+  a.ll_slot = h->em_slot;
+  a.expert_offset = h->em_offset;
+  a.expert_count = h->em_count;
+  a.recv_src_idx = recv_src_idx;
+  a.recv_weights = recv_weights;
+  a.scales_ld = scales_ld;
+  a.recv_x = recv_x;
+  a.recv_scales = recv_scales;
+  a.err = h->err;
+  const int sns = h->scatter_ns[fp8 ? 1 : 0][ep::kSrcExpertMajor], snc = h->scatter_nc[fp8 ? 1 : 0][ep::kSrcExpertMajor];
+  const int blocks = grid_for(h, 1, num_sms, T, 1);
+  ep::launch_scatter(a, fp8, ep::kSrcExpertMajor, blocks, sns, snc, s);
+  if (h->debug)
+    std::fprintf(stderr, "[ep] em dispatch %s T=%d: TMA scatter %d blocks, %d stages, %d consumers\n",
+                 fp8 ? "fp8" : "bf16", T, blocks, sns, snc);
+  return cuda_status(cudaGetLastError(), "k_scatter(em) launch");
+}
+
+}  // namespace
+
+ep_status_t ep_em_layout_and_dispatch(ep_handle_t h, const void* topk_idx, int T, const void* x,
+                                      const float* topk_weights, ep_dtype_t dtype, int align, void* recv_x,
+                                      float* recv_scales, int64_t scales_ld, int64_t cap, int* recv_src_idx,
+                                      float* recv_weights, int num_sms, ep_stream_t stream) {
+  if (!h) return EP_ERR_INVALID_ARG;
+  if (T < 0 || T % h->R != 0 || T > h->Tmax || (T > 0 && (!topk_idx || !x)) || align < 1 || align > (1 << 16))
+    return EP_ERR_INVALID_ARG;
+  if (static_cast<long long>(T) * h->k + static_cast<long long>(h->E) * (align - 1) > (1LL << 31) - 1)
+    return EP_ERR_INVALID_ARG;
+  if (!ids_aligned(h, topk_idx) || (x && !aligned16(x))) return EP_ERR_INVALID_ARG;
+  ep_status_t st = em_check_outputs(h, dtype, topk_weights, recv_x, recv_scales, scales_ld, cap, recv_src_idx,
+                                    recv_weights);
+  if (st != EP_OK) return st;
+  if ((st = check_device(h)) != EP_OK) return st;
+  const bool fp8 = dtype == EP_FP8_E4M3;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    cudaError_t e = cudaMemsetAsync(h->em_count, 0, sizeof(int) * h->E, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->em_offset, 0, sizeof(int) * (h->E + 1), s);
+    if ((st = cuda_status(e, "em memset")) != EP_OK) return st;
+    h->T_em = 0;
+    return EP_OK;
+  }
+  int fblocks = 0, fns = 0, fnc = 0;
+  ep::fused_config(ep::kSrcExpertMajor, fp8, T, h->R, h->E, h->k, h->kmax, h->H, sms_for(h, num_sms), h->smem_optin,
+                   &fblocks, &fns, &fnc);
+  if (fblocks > 0) {
+    ep::FusedArgs f = fused_args(h, topk_idx, static_cast<const uint16_t*>(x), topk_weights, T);
+    f.agg = h->fused_agg;
+    f.ll_idx = h->em_idx;
+    f.ll_slot = h->em_slot;
+    f.recv_count = h->em_count;
+    f.align = align;
+    f.expert_offset = h->em_offset;
+    f.cap = cap;
+    f.recv_src_idx = recv_src_idx;
+    f.recv_weights = recv_weights;
+    f.scales_ld = scales_ld;
+    f.recv_x = recv_x;
+    f.recv_scales = recv_scales;
+    if ((st = cuda_status(ep::launch_fused(f, fp8, ep::kSrcExpertMajor, fblocks, fns, fnc, s),
+                          "k_route_scatter(em) launch")) != EP_OK)
+      return st;
+    if (h->debug)
+      std::fprintf(stderr, "[ep] em layout+dispatch T=%d: fused, %d blocks, %d stages, %d consumers\n", T, fblocks,
+                   fns, fnc);
+    h->T_em = T;
+    return EP_OK;
+  }
+  // per-expert slots on layout-sized chunks, the group offsets, then the rows
+  RouteParams p = route_params(h, topk_idx, T, h->layout_CT, h->em_flags, h->tickets + 2);
+  ep::LowLatencyOutPtrs ro{h->em_count, h->em_idx, h->em_slot, INT_MAX};
+  ep::launch_ll_route(p, ro, h->ll_route_smem, s);
+  if ((st = cuda_status(cudaGetLastError(), "k_ll_route(em) launch")) != EP_OK) return st;
+  ep::launch_em_offsets(h->em_count, h->E, align, h->em_offset, s);
+  if ((st = cuda_status(cudaGetLastError(), "k_em_offsets launch")) != EP_OK) return st;
+  h->T_em = T;
+  return em_scatter(h, x, topk_weights, fp8, recv_x, recv_scales, scales_ld, cap, recv_src_idx, recv_weights,
+                    num_sms, s);
+}
+
+ep_status_t ep_em_dispatch(ep_handle_t h, const void* x, const float* topk_weights, ep_dtype_t dtype, void* recv_x,
+                           float* recv_scales, int64_t scales_ld, int64_t cap, int* recv_src_idx,
+                           float* recv_weights, int num_sms, ep_stream_t stream) {
+  if (!h) return EP_ERR_INVALID_ARG;
+  if (h->T_em < 0) return EP_ERR_STATE;
+  const int T = h->T_em;
+  if ((T > 0 && !x) || (x && !aligned16(x))) return EP_ERR_INVALID_ARG;
+  ep_status_t st = em_check_outputs(h, dtype, topk_weights, recv_x, recv_scales, scales_ld, cap, recv_src_idx,
+                                    recv_weights);
+  if (st != EP_OK) return st;
+  if ((st = check_device(h)) != EP_OK) return st;
+  if (T == 0) return EP_OK;
+  return em_scatter(h, x, topk_weights, dtype == EP_FP8_E4M3, recv_x, recv_scales, scales_ld, cap, recv_src_idx,
+                    recv_weights, num_sms, reinterpret_cast<cudaStream_t>(stream));
+}
+
+ep_status_t ep_em_get_layout(ep_handle_t h, int* num_recv_tokens_per_expert, int* expert_offset, ep_stream_t stream) {
+  if (!h) return EP_ERR_INVALID_ARG;
+  if (h->T_em < 0) return EP_ERR_STATE;
+  ep_status_t st = check_device(h);
+  if (st != EP_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int* hp = h->host;
+  cudaError_t e = cudaMemcpyAsync(hp, h->err, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(hp + 1, h->em_count, sizeof(int) * h->E, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(hp + 1 + h->E, h->em_offset, sizeof(int) * (h->E + 1), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if ((st = cuda_status(e, "ep_em_get_layout")) != EP_OK) return st;
+  if (num_recv_tokens_per_expert) std::memcpy(num_recv_tokens_per_expert, hp + 1, sizeof(int) * h->E);
+  if (expert_offset) std::memcpy(expert_offset, hp + 1 + h->E, sizeof(int) * (h->E + 1));
+  return static_cast<ep_status_t>(hp[0]);
+}
+
+ep_status_t ep_em_combine(ep_handle_t h, const void* y, int64_t y_rows, void* out, int num_sms, ep_stream_t stream) {
+  if (!h) return EP_ERR_INVALID_ARG;
+  if (h->T_em < 0) return EP_ERR_STATE;
+  const int T = h->T_em;
+  if (y_rows < 0 || (T > 0 && (!out || (y_rows > 0 && !y)))) return EP_ERR_INVALID_ARG;
+  if ((y && !aligned16(y)) || (out && !aligned16(out))) return EP_ERR_INVALID_ARG;
+  ep_status_t st = check_device(h);
+  if (st != EP_OK) return st;
+  if (T == 0) return EP_OK;
+  ep::CombineArgs a{};
+  a.y = y;
+  a.out = static_cast<uint16_t*>(out);
+  a.y_rows = y_rows;
+  a.T = T;
+  a.H = h->H;
+  a.k = h->k;
+  a.kmax = h->kmax;
+  a.R = h->R;
+  a.E = h->E;
+  a.ent_idx = h->em_idx;
+  a.ent_slot = h->em_slot;
+  a.expert_offset = h->em_offset;
+  a.err = h->err;
+  const int blocks = grid_for(h, h->occ_combine[3], num_sms, T * ((h->H + 1023) / 1024), ep::combine_threads() / 32);
+  ep::launch_combine(a, ep::kSrcExpertMajor, false, blocks, reinterpret_cast<cudaStream_t>(stream));
+  if (h->debug) std::fprintf(stderr, "[ep] em combine T=%d: %d blocks\n", T, blocks);
+  return cuda_status(cudaGetLastError(), "k_combine(em) launch");
+}
+
+ep_status_t ep_get_buffer_size_hint(int R, int E, int k, int H, int max_tpr, ep_dtype_t dtype, ep_layout_t layout,
+                                    int align, int64_t* rows, int64_t* bytes) {
+  if (R < 1 || E < 1 || E % R != 0 || k < 1 || k > 32 || H < 128 || H % 128 != 0 || max_tpr < 1 ||
+      (dtype != EP_BF16 && dtype != EP_FP8_E4M3) || (layout == EP_LAYOUT_EXPERT_MAJOR && align < 1))
+    return EP_ERR_INVALID_ARG;
+  const bool fp8 = dtype == EP_FP8_E4M3;
+  const long long T = static_cast<long long>(R) * max_tpr;
+  const long long G = H / 128;
+  const long long row_bytes = fp8 ? H + 4 * G : 2LL * H;
+  long long n = 0, b = 0;
+  switch (layout) {
+    case EP_LAYOUT_RANK_MAJOR:
+      // at most min(k, R) destination ranks per token; per row the payload,
+      // its scales, the source index and the k local ids and weights
+      n = T * (k < R ? k : R);
+      b = n * (row_bytes + 4 + 8LL * k);
+      break;
+    case EP_LAYOUT_LOW_LATENCY:
+      // [E][M][H] with M = R * max_tokens_per_rank, plus src_info and counts
+      n = static_cast<long long>(E) * T;
+      b = n * (row_bytes + 4) + 4LL * E;
+      break;
+    case EP_LAYOUT_EXPERT_MAJOR: {
+      // every entry unmasked, and each group padded by at most align - 1;
+      // scales [G][ld] with ld = rows rounded up to 4
+      n = T * k + static_cast<long long>(E) * (align - 1);
+      const long long ld = (n + 3) / 4 * 4;
+      b = n * (fp8 ? H : 2LL * H) + (fp8 ? 4 * G * ld : 0) + n * 8;
+      break;
+    }
+    default:
+      return EP_ERR_INVALID_ARG;
+  }
+  if (rows) *rows = n;
+  if (bytes) *bytes = b;
+  return EP_OK;
 }
 
 ep_status_t ep_handle_set_topk_idx_bits(ep_handle_t h, int bits) {

@@ -10,15 +10,22 @@
 //                   token's ranks as a 64-bit mask (R <= 64), one ballot per
 //                   distinct rank in a 32-token batch; expert counts by
 //                   shared-memory atomics;
-//   low latency  -- per (token, k) entry and expert: __match_any_sync within a
-//                   32-entry batch, per-warp running counts in shared memory.
+//   low latency / expert-major -- per (token, k) entry and expert:
+//                   __match_any_sync within a 32-entry batch, per-warp running
+//                   counts in shared memory.
 // Each block publishes its counts, all blocks meet at one bounded grid
 // barrier (co-residency guaranteed by the cooperative launch), and each block
-// sums its predecessors' counts into exclusive prefixes (block 0 also forms
-// the totals).  The destination rows are then known and the consumer warps
-// quantise / store the rows exactly as k_scatter does.  Rows and slots come
-// out identical to the separate routing kernels: (source rank, token) order
-// per rank, (source rank, token, k) order per expert.
+// sums its predecessors' counts into exclusive prefixes.  The destination
+// rows are then known and the consumer warps quantise / store the rows
+// exactly as k_scatter does; per-expert totals, which nothing waits for, are
+// formed after the rows.  Rows and slots come out identical to the separate
+// routing kernels: (source rank, token) order per rank, (source rank, token,
+// k) order per expert.  The expert-major ("GEMM") layout of the V2 release
+// notes in "DeepSeek công bố thư viện mã nguồn mở DeepEP ..."
+// (vi.news.hada.io, "Những thay đổi chính của bản phát hành V2") packs those
+// per-expert slots one expert after another, each expert's group starting at
+// a multiple of the alignment; every block forms the group offsets itself
+// from the totals.
 #include <climits>
 
 #include "ep_internal.h"
@@ -30,6 +37,11 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" : : "r"(nthreads) : "memory");
 }
 
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -40,19 +52,22 @@ __device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
 }
 
 // Grid-wide barrier among the consumer warps of all blocks.  Word 0 counts
-// arrivals, word 1 is the generation; the last arrival resets the count and
-// bumps the generation.  Bounded: gives up after kSpinLimit polls (latched
-// kErrTimeout).
-__device__ inline void grid_sync(unsigned* words, unsigned nblocks, int* err, int nthreads) {
-  __threadfence();
+// arrivals, word 1 is the generation, which thread 32 read (into g) when the
+// kernel started: it cannot change before every block, this one included,
+// has arrived.  The block's writes are ordered before thread 32's fence by the
+// block barrier, the fence before its arrival; the last arrival releases the
+// others by bumping the generation, then resets the count for the next launch
+// (nothing reads it again in this one).  Bounded: gives up after kSpinLimit
+// polls (latched kErrTimeout).
+__device__ inline void grid_sync(unsigned* words, unsigned g, unsigned nblocks, int* err, int nthreads) {
   consumer_sync(nthreads);
   if (threadIdx.x == 32) {
-    const unsigned g = ld_acquire_u32(words + 1);
+    __threadfence();
     const unsigned arrived = atomicAdd(words, 1u);
     if (arrived == nblocks - 1) {
-      atomicExch(words, 0u);
       __threadfence();
       st_release_u32(words + 1, g + 1);
+      atomicExch(words, 0u);
     } else {
       int it = 0;
       while (ld_acquire_u32(words + 1) == g) {
@@ -89,26 +104,96 @@ __device__ __forceinline__ void column_sums(const int* agg, int NK, int col, int
   *all = a;
 }
 
+// Columns [0, ncols) of the per-block counts (row q = block q's counts, NK
+// ints per row): excl[c] = the sum over blocks q < b and, if `all` is given,
+// all[c] = the sum over every block.  tpc threads share a column (a power of
+// two up to 32, so they sit in one warp); each thread issues its loads 32 at a
+// time before adding any, then one shuffle reduction per column: a column
+// costs about one L2 round trip per 32 * tpc blocks.
+__device__ inline void column_sums_par(const int* agg, int NK, int ncols, int nb, int b, int* excl, int* all, int nct,
+                                       int ct) {
+  int tpc = 32;
+  while (tpc > 1 && tpc * ncols > nct) tpc >>= 1;
+  const int groups = nct / tpc;
+  const int sub = ct & (tpc - 1);
+  const int qend = all ? nb : b;
+  for (int c0 = 0; c0 < ncols; c0 += groups) {  // the same trip count in every thread
+    const int c = c0 + ct / tpc;
+    const bool valid = c < ncols;
+    int e = 0, s = 0;
+    if (valid) {
+      for (int q0 = sub; q0 < qend; q0 += 32 * tpc) {
+        int v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int q = q0 + j * tpc;
+          v[j] = q < qend ? __ldcg(agg + static_cast<size_t>(q) * NK + c) : 0;
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          s += v[j];
+          if (q0 + j * tpc < b) e += v[j];
+        }
+      }
+    }
+    for (int d = tpc >> 1; d >= 1; d >>= 1) {
+      e += __shfl_xor_sync(kFullMask, e, d);
+      s += __shfl_xor_sync(kFullMask, s, d);
+    }
+    if (valid && sub == 0) {
+      excl[c] = e;
+      if (all) all[c] = s;
+    }
+  }
+}
+
 // Routing tables in shared memory (int32 unless noted).
-__host__ __device__ inline size_t fused_route_bytes(bool low_latency, int R, int E, int kmax, int kp, int tpb, int nc) {
-  if (!low_latency)
+__host__ __device__ inline size_t fused_route_bytes(int mode, int R, int E, int kmax, int kp, int tpb, int nc) {
+  if (mode == kSrcRanks)
     return 8 * static_cast<size_t>(tpb)                        // token rank masks (u64)
            + 8 * static_cast<size_t>(tpb) * kmax               // (rank, row) per token
            + 4 * static_cast<size_t>(tpb) * kmax               // local rows
            + 4 * (static_cast<size_t>(nc) * R + E + 3 * (R + 1) + 4);
   const size_t ni = static_cast<size_t>(tpb) * kp;
-  return 8 * ni + 4 * (static_cast<size_t>(nc) * E + E + 4);
+  const size_t em = mode == kSrcExpertMajor ? 2 * static_cast<size_t>(E) + 1 + 32 : 0;  // totals, offsets, scan
+  return 8 * ni + 4 * (static_cast<size_t>(nc) * E + E + 4 + em);
 }
 
-__host__ __device__ inline size_t fused_smem_bytes(bool low_latency, bool fp8, int R, int E, int kmax, int kp,
-                                                   int tpb, int nc, int ns, int H) {
-  const size_t route = (fused_route_bytes(low_latency, R, E, kmax, kp, tpb, nc) + 127) & ~static_cast<size_t>(127);
+// Exclusive scan of one value per consumer thread (in thread order) over
+// the block's consumer threads; `wsum` holds NC ints.  Returns the thread's
+// exclusive prefix and the total in *total.
+__device__ inline int consumer_exclusive_scan(int v, int* wsum, int nct, int* total) {
+  const int lane = threadIdx.x & 31;
+  const int cw = (threadIdx.x >> 5) - 1;
+  int inc = v;
+  for (int d = 1; d < 32; d <<= 1) {
+    const int u = __shfl_up_sync(kFullMask, inc, d);
+    if (lane >= d) inc += u;
+  }
+  if (lane == 31) wsum[cw] = inc;
+  consumer_sync(nct);
+  int base = 0, all = 0;
+  for (int w = 0; w < nct / 32; ++w) {
+    const int s = wsum[w];
+    if (w < cw) base += s;
+    all += s;
+  }
+  consumer_sync(nct);
+  *total = all;
+  return base + inc - v;
+}
+
+__host__ __device__ inline size_t fused_smem_bytes(int mode, bool fp8, int R, int E, int kmax, int kp, int tpb,
+                                                   int nc, int ns, int H) {
+  const size_t route = (fused_route_bytes(mode, R, E, kmax, kp, tpb, nc) + 127) & ~static_cast<size_t>(127);
   const size_t qb = static_cast<size_t>(H) + ((4 * static_cast<size_t>(H / 128) + 15) & ~15ull);
   return route + 16 * static_cast<size_t>(ns) + static_cast<size_t>(ns) * 2 * H + (fp8 ? nc * qb : 0);
 }
 
-template <bool kFP8, bool kLL>
+template <bool kFP8, int kMode>
 __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_scatter(FusedArgs a, int NS) {
+  constexpr bool kLL = kMode != kSrcRanks;        // per-entry routing (low latency, expert-major)
+  constexpr bool kEM = kMode == kSrcExpertMajor;  // packed expert groups
   extern __shared__ __align__(128) unsigned char smem[];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -130,7 +215,7 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
   unsigned long long* tmask = nullptr;
   int2* tdst = nullptr;
   int *tlocal = nullptr, *cnt = nullptr, *hist = nullptr, *so = nullptr, *excl = nullptr, *tot = nullptr;
-  int *item_e = nullptr, *item_slot = nullptr;
+  int *item_e = nullptr, *item_slot = nullptr, *etot = nullptr, *eoff = nullptr, *wsum = nullptr;
   if (!kLL) {
     tmask = reinterpret_cast<unsigned long long*>(p);
     p += 8 * static_cast<size_t>(tpb);
@@ -148,8 +233,13 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
     item_slot = item_e + tpb * kp;
     cnt = item_slot + tpb * kp;        // [NC][E], then per-warp prefixes
     excl = cnt + NC * E;               // [E]
+    if (kEM) {
+      etot = excl + E + 4;             // [E] totals
+      eoff = etot + E;                 // [E+1] group offsets
+      wsum = eoff + E + 1;             // [32] scan scratch
+    }
   }
-  unsigned char* sbase = smem + ((fused_route_bytes(kLL, R, E, kmax, kp, tpb, NC) + 127) & ~static_cast<size_t>(127));
+  unsigned char* sbase = smem + ((fused_route_bytes(kMode, R, E, kmax, kp, tpb, NC) + 127) & ~static_cast<size_t>(127));
   uint64_t* full = reinterpret_cast<uint64_t*>(sbase);
   uint64_t* empty = full + NS;
   unsigned char* stage0 = reinterpret_cast<unsigned char*>(empty + NS);
@@ -179,6 +269,10 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
   }
 
   const int cw = warp - 1;  // consumer warp
+  // the grid barrier's generation: written last by the previous launch, so a
+  // relaxed load sees it (and, unlike an acquire, does not hold back the loads
+  // that follow)
+  const unsigned gen = threadIdx.x == 32 ? ld_relaxed_u32(a.barrier + 1) : 0u;
   const unsigned lt = lanemask_lt();
   // ---------------------------------------------------------------- phase 1: rank the block's tokens
   if (!kLL) {
@@ -287,10 +381,10 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
   }
 
   // ---------------------------------------------------------------- phase 2: prefixes over blocks
-  grid_sync(a.barrier, static_cast<unsigned>(nb), a.err, nct);
+  grid_sync(a.barrier, gen, static_cast<unsigned>(nb), a.err, nct);
   const int NK = kLL ? E : R + E;
   if (!kLL) {
-    for (int col = ct; col < R; col += nct) column_sums(a.agg, NK, col, nb, b, excl + col, tot + col);
+    column_sums_par(a.agg, NK, R, nb, b, excl, tot, nct, ct);
     consumer_sync(nct);
     if (cw == 0) {  // exclusive scan of the rank totals -> region offsets
       const int v = lane < R ? tot[lane] : 0;
@@ -343,11 +437,23 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
       }
     }
   } else {
-    for (int col = ct; col < E; col += nct) {
-      int all;
-      column_sums(a.agg, NK, col, nb, b, excl + col, &all);
-    }
+    column_sums_par(a.agg, NK, E, nb, b, excl, kEM ? etot : nullptr, nct, ct);
     consumer_sync(nct);
+    if (kEM) {
+      // group offsets: each consumer thread takes a contiguous run of experts
+      const int per = (E + nct - 1) / nct;
+      const int e0 = min(E, ct * per), e1 = min(E, e0 + per);
+      int run = 0;
+      for (int e = e0; e < e1; ++e) run += (etot[e] + a.align - 1) / a.align * a.align;
+      int total;
+      int at = consumer_exclusive_scan(run, wsum, nct, &total);
+      for (int e = e0; e < e1; ++e) {
+        eoff[e] = at;
+        at += (etot[e] + a.align - 1) / a.align * a.align;
+      }
+      if (ct == 0) eoff[E] = total;
+      consumer_sync(nct);
+    }
     const int NI = tpb << a.kp_log2;
     const int ipw = (((NI + NC - 1) / NC) + 31) & ~31;
     for (int i = ct; i < n_own * kp; i += nct) {
@@ -359,13 +465,17 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
       int slot = -1;
       if (e >= 0) {
         slot = excl[e] + cnt[(i / ipw) * E + e] + item_slot[i];
-        if (slot >= a.M) {
+        if (!kEM && slot >= a.M) {
           latch_error(a.err, kErrCapacity);
           slot = -1;
         }
       }
       a.ll_idx[static_cast<size_t>(t) * k + j] = e;
       a.ll_slot[static_cast<size_t>(t) * k + j] = slot;
+      if (kEM && slot >= 0 && static_cast<long long>(eoff[e]) + slot >= a.cap) {
+        latch_error(a.err, kErrCapacity);  // the row does not fit the receive buffer
+        slot = -1;
+      }
       item_slot[i] = slot;
     }
   }
@@ -401,7 +511,8 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
     } else if (lane < k) {
       const int ee = item_e[(i << a.kp_log2) + lane];
       const int sl = item_slot[(i << a.kp_log2) + lane];
-      if (ee >= 0 && sl >= 0) row = static_cast<long long>(ee) * a.M + sl;
+      if (ee >= 0 && sl >= 0) row = kEM ? static_cast<long long>(eoff[ee]) + sl : static_cast<long long>(ee) * a.M + sl;
+      if (kEM && row >= 0 && a.recv_weights) w = a.topk_weights[static_cast<size_t>(t) * k + lane];
     }
     const unsigned dmask = __ballot_sync(kFullMask, row >= 0);
     const bool landed = mbar_wait(full + s, static_cast<uint32_t>((i / NS) & 1), a.err);
@@ -421,7 +532,10 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
         m &= m - 1;
         const long long rr = __shfl_sync(kFullMask, row, sl);
         if (lane == 0) bulk_store(static_cast<uint8_t*>(a.recv_x) + rr * H, qd, static_cast<uint32_t>(H));
-        for (int g = lane; g < G; g += 32) a.recv_scales[rr * G + g] = sd[g];
+        if (kEM)
+          for (int g = lane; g < G; g += 32) a.recv_scales[g * a.scales_ld + rr] = sd[g];
+        else
+          for (int g = lane; g < G; g += 32) a.recv_scales[rr * G + g] = sd[g];
       }
       if (lane == 0) bulk_commit();
     } else {
@@ -454,13 +568,32 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
           if (a.recv_topk_weights) a.recv_topk_weights[rr * k + lane] = here ? w : 0.0f;
         }
       }
+    } else if (kEM && row >= 0) {
+      if (a.recv_src_idx) a.recv_src_idx[row] = t;
+      if (a.recv_weights) a.recv_weights[row] = w;
     } else if (kLL && a.recv_src_info && row >= 0) {
       a.recv_src_info[row] = t;
     }
   }
+  if (kEM) {
+    // padding rows of the groups this block owns (experts b, b + nb, ...):
+    // no source token, weight 0; and the group offsets and counts
+    for (int e = b; e < E; e += nb) {
+      const long long end = min(static_cast<long long>(eoff[e + 1]), a.cap);
+      for (long long rw = static_cast<long long>(eoff[e]) + etot[e] + ct; rw < end; rw += nct) {
+        if (a.recv_src_idx) a.recv_src_idx[rw] = -1;
+        if (a.recv_weights) a.recv_weights[rw] = 0.0f;
+      }
+      if (ct == 0) {
+        a.expert_offset[e] = eoff[e];
+        a.recv_count[e] = etot[e];
+      }
+    }
+    if (b == 0 && ct == 0) a.expert_offset[E] = eoff[E];
+  }
   // per-expert totals (outputs only, nothing above waits for them): block b
   // forms the totals of experts e = b, b + nb, ...
-  for (int e = b + ct * nb; e < E; e += nct * nb) {
+  for (int e = b + ct * nb; !kEM && e < E; e += nct * nb) {
     int ex, all;
     column_sums(a.agg, NK, (kLL ? 0 : R) + e, nb, 0, &ex, &all);
     if (kLL) {
@@ -476,17 +609,17 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
 // Blocks, stages and consumers for the fused kernel; blocks = 0 when it does
 // not apply (R > 64 in normal mode, too many (token, k) entries per block,
 // rows too long for two stages).
-void fused_config(bool low_latency, bool fp8, int T, int R, int E, int k, int kmax, int H, int sms,
-                  size_t smem_limit, int* blocks, int* NS, int* NC) {
+void fused_config(int mode, bool fp8, int T, int R, int E, int k, int kmax, int H, int sms, size_t smem_limit,
+                  int* blocks, int* NS, int* NC) {
   *blocks = *NS = *NC = 0;
-  if (T <= 0 || (!low_latency && R > 64)) return;
+  if (T <= 0 || (mode == kSrcRanks && R > 64)) return;
   int kp = 1;
   while (kp < k) kp <<= 1;
   const int nb = sms;
   const int tpb = fused_tokens_per_block(T, nb);
   if (tpb * kp > kFusedMaxItems) return;
   for (int nc = fp8 ? kScatterMaxConsumers : 4; nc >= 1; --nc) {
-    const size_t fixed = fused_smem_bytes(low_latency, fp8, R, E, kmax, kp, tpb, nc, 0, H);
+    const size_t fixed = fused_smem_bytes(mode, fp8, R, E, kmax, kp, tpb, nc, 0, H);
     if (fixed >= smem_limit) continue;
     int ns = static_cast<int>((smem_limit - fixed) / (16 + 2 * static_cast<size_t>(H)));
     if (ns > 32) ns = 32;
@@ -500,10 +633,12 @@ void fused_config(bool low_latency, bool fp8, int T, int R, int E, int k, int km
 }
 
 cudaError_t configure_fused(size_t smem_limit) {
-  const void* ks[4] = {reinterpret_cast<const void*>(k_route_scatter<false, false>),
-                       reinterpret_cast<const void*>(k_route_scatter<true, false>),
-                       reinterpret_cast<const void*>(k_route_scatter<false, true>),
-                       reinterpret_cast<const void*>(k_route_scatter<true, true>)};
+  const void* ks[6] = {reinterpret_cast<const void*>(k_route_scatter<false, kSrcRanks>),
+                       reinterpret_cast<const void*>(k_route_scatter<true, kSrcRanks>),
+                       reinterpret_cast<const void*>(k_route_scatter<false, kSrcLowLatency>),
+                       reinterpret_cast<const void*>(k_route_scatter<true, kSrcLowLatency>),
+                       reinterpret_cast<const void*>(k_route_scatter<false, kSrcExpertMajor>),
+                       reinterpret_cast<const void*>(k_route_scatter<true, kSrcExpertMajor>)};
   for (const void* kk : ks) {
     cudaError_t e =
         cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_limit));
@@ -512,12 +647,11 @@ cudaError_t configure_fused(size_t smem_limit) {
   return cudaSuccess;
 }
 
-cudaError_t launch_fused(const FusedArgs& a, bool fp8, bool low_latency, int blocks, int NS, int NC,
-                         cudaStream_t stream) {
+cudaError_t launch_fused(const FusedArgs& a, bool fp8, int mode, int blocks, int NS, int NC, cudaStream_t stream) {
   int kp = 1;
   while (kp < a.k) kp <<= 1;
   const int tpb = fused_tokens_per_block(a.T, blocks);
-  const size_t smem = fused_smem_bytes(low_latency, fp8, a.R, a.E, a.kmax, kp, tpb, NC, NS, a.H);
+  const size_t smem = fused_smem_bytes(mode, fp8, a.R, a.E, a.kmax, kp, tpb, NC, NS, a.H);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
@@ -528,11 +662,14 @@ cudaError_t launch_fused(const FusedArgs& a, bool fp8, bool low_latency, int blo
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (low_latency)
-    return fp8 ? cudaLaunchKernelEx(&cfg, k_route_scatter<true, true>, a, NS)
-               : cudaLaunchKernelEx(&cfg, k_route_scatter<false, true>, a, NS);
-  return fp8 ? cudaLaunchKernelEx(&cfg, k_route_scatter<true, false>, a, NS)
-             : cudaLaunchKernelEx(&cfg, k_route_scatter<false, false>, a, NS);
+  if (mode == kSrcLowLatency)
+    return fp8 ? cudaLaunchKernelEx(&cfg, k_route_scatter<true, kSrcLowLatency>, a, NS)
+               : cudaLaunchKernelEx(&cfg, k_route_scatter<false, kSrcLowLatency>, a, NS);
+  if (mode == kSrcExpertMajor)
+    return fp8 ? cudaLaunchKernelEx(&cfg, k_route_scatter<true, kSrcExpertMajor>, a, NS)
+               : cudaLaunchKernelEx(&cfg, k_route_scatter<false, kSrcExpertMajor>, a, NS);
+  return fp8 ? cudaLaunchKernelEx(&cfg, k_route_scatter<true, kSrcRanks>, a, NS)
+             : cudaLaunchKernelEx(&cfg, k_route_scatter<false, kSrcRanks>, a, NS);
 }
 
 }  // namespace ep

@@ -101,7 +101,7 @@ const void* combine_kernel(int src, bool fp8);
 constexpr int kScatterMaxConsumers = 8;
 struct ScatterArgs {
   const uint16_t* x;           // [T][H] bf16
-  int T, H, k, kmax, El, R;
+  int T, H, k, kmax, El, R, E;
   // normal destinations
   const int2* dst;             // [T][kmax]
   const int* rank_offset;      // [R+1]
@@ -116,6 +116,12 @@ struct ScatterArgs {
   const int* ll_slot;          // [T][k]
   int M;
   int* recv_src_info;
+  // expert-major destinations (ll_idx / ll_slot above are the entries'
+  // expert and slot in the expert; recv_src_idx is the row's source token)
+  const int* expert_offset;    // [E+1]
+  const int* expert_count;     // [E]
+  float* recv_weights;         // [cap] or null
+  long long scales_ld;         // scales stored [G][scales_ld]
   // outputs
   void* recv_x;
   float* recv_scales;
@@ -123,11 +129,10 @@ struct ScatterArgs {
 };
 // NS row stages and NC consumer warps that fit `smem_limit` (NS = 0: the
 // rows are too long for the bulk-copy staging).
-void scatter_config(int H, int R, bool fp8, bool low_latency, size_t smem_limit, int* NS, int* NC);
-size_t scatter_smem_bytes(int H, int R, bool fp8, bool low_latency, int NS, int NC);
+void scatter_config(int H, int R, int E, bool fp8, int mode, size_t smem_limit, int* NS, int* NC);
+size_t scatter_smem_bytes(int H, int R, int E, bool fp8, int mode, int NS, int NC);
 cudaError_t configure_scatter(size_t smem_limit);
-void launch_scatter(const ScatterArgs& a, bool fp8, bool low_latency, int blocks, int NS, int NC,
-                    cudaStream_t stream);
+void launch_scatter(const ScatterArgs& a, bool fp8, int mode, int blocks, int NS, int NC, cudaStream_t stream);
 
 // Fused routing + dispatch (cooperative launch, one block per SM).
 constexpr int kFusedMaxItems = 4096;  // (token, k) entries a block may own
@@ -150,24 +155,33 @@ struct FusedArgs {
   int* recv_src_idx;
   int* recv_topk_idx;
   float* recv_topk_weights;
-  // low-latency mode
+  // low-latency and expert-major modes: per entry expert id and slot in
+  // the expert (the handle's state); per expert rows filled
   int* ll_idx;
   int* ll_slot;
   int* recv_count;
   int* recv_src_info;
+  // expert-major mode: group alignment, the handle's group offsets [E+1],
+  // per-row top-k weight, scales stored [G][scales_ld] (recv_src_idx above
+  // is the per-row source token)
+  int align;
+  int* expert_offset;
+  float* recv_weights;
+  long long scales_ld;
   // rows
   void* recv_x;
   float* recv_scales;
 };
-void fused_config(bool low_latency, bool fp8, int T, int R, int E, int k, int kmax, int H, int sms,
-                  size_t smem_limit, int* blocks, int* NS, int* NC);
+void fused_config(int mode, bool fp8, int T, int R, int E, int k, int kmax, int H, int sms, size_t smem_limit,
+                  int* blocks, int* NS, int* NC);
 cudaError_t configure_fused(size_t smem_limit);
-cudaError_t launch_fused(const FusedArgs& a, bool fp8, bool low_latency, int blocks, int NS, int NC,
-                         cudaStream_t stream);
+cudaError_t launch_fused(const FusedArgs& a, bool fp8, int mode, int blocks, int NS, int NC, cudaStream_t stream);
 
 // Low-latency routing only (slots, counts); the rows move with k_scatter.
 void launch_ll_route(const RouteParams& p, const LowLatencyOutPtrs& o, size_t smem, cudaStream_t stream);
 cudaError_t configure_ll_route(size_t smem);
+// Expert-major group offsets [E+1] from per-expert counts (one block).
+void launch_em_offsets(const int* count, int E, int align, int* offset, cudaStream_t stream);
 
 // Fused low-latency dispatch: routing phase + per-chunk scatter.
 struct LowLatencyOut {

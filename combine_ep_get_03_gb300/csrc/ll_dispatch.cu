@@ -119,6 +119,41 @@ void launch_ll_route(const RouteParams& p, const LowLatencyOutPtrs& o, size_t sm
   (void)launch_kernel(k_ll_route, dim3(p.C), dim3(kRouteThreads), smem, stream, p, o);
 }
 
+// Expert-major group offsets from the per-expert counts: offset[e] = sum over
+// e' < e of count[e'] rounded up to a multiple of align; offset[E] = total.
+// One block: each thread takes a contiguous run of experts, then a block scan.
+constexpr int kEmOffsetThreads = 1024;
+__global__ void __launch_bounds__(kEmOffsetThreads) k_em_offsets(const int* count, int E, int align, int* offset) {
+  __shared__ int wsum[kEmOffsetThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per = (E + kEmOffsetThreads - 1) / kEmOffsetThreads;
+  const int e0 = min(E, static_cast<int>(threadIdx.x) * per), e1 = min(E, e0 + per);
+  int run = 0;
+  for (int e = e0; e < e1; ++e) run += (count[e] + align - 1) / align * align;
+  int inc = run;
+  for (int d = 1; d < 32; d <<= 1) {
+    const int u = __shfl_up_sync(kFullMask, inc, d);
+    if (lane >= d) inc += u;
+  }
+  if (lane == 31) wsum[warp] = inc;
+  __syncthreads();
+  int base = 0, total = 0;
+  for (int w = 0; w < kEmOffsetThreads / 32; ++w) {
+    if (w < warp) base += wsum[w];
+    total += wsum[w];
+  }
+  int at = base + inc - run;
+  for (int e = e0; e < e1; ++e) {
+    offset[e] = at;
+    at += (count[e] + align - 1) / align * align;
+  }
+  if (threadIdx.x == 0) offset[E] = total;
+}
+
+void launch_em_offsets(const int* count, int E, int align, int* offset, cudaStream_t stream) {
+  (void)launch_kernel(k_em_offsets, dim3(1), dim3(kEmOffsetThreads), 0, stream, count, E, align, offset);
+}
+
 cudaError_t configure_ll_route(size_t smem) {
   return cudaFuncSetAttribute(k_ll_route, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
 }

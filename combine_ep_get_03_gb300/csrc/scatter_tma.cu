@@ -12,7 +12,11 @@
 //
 // Destinations:  normal  -- the handle's (rank, row-in-rank) list + the
 //                           rank's region offset (the layout's output);
-//                low latency -- expert e's row `slot` in [E][M][H].
+//                low latency -- expert e's row `slot` in [E][M][H];
+//                expert-major -- row expert_offset[e] + slot of the packed
+//                           expert groups; fp8 scales stored group-major
+//                           [G][scales_ld]; padding rows of each group get
+//                           source -1 and weight 0.
 //
 // FP8: a lane quantises whole 128-channel groups (quantize_row_smem), so a
 // token row costs one warp-wide pair of divisions per 32 groups and no
@@ -23,7 +27,8 @@
 namespace ep {
 
 // Block layout (dynamic shared memory):
-//   [rank_offset: R+1 ints, normal mode][full[NS], empty[NS] mbarriers]
+//   [rank_offset: R+1 ints (normal) | expert_offset: E+1 ints (expert-major)]
+//   [full[NS], empty[NS] mbarriers]
 //   [NS row stages of 2H bytes][NC quantised-row buffers of H + scales (FP8)]
 // Warp 0 is the producer: lane 0 streams the block's token rows into the
 // stages with bulk loads (full[s] counts the bytes).  Warps 1..NC are
@@ -31,17 +36,22 @@ namespace ep {
 // its stage, quantises it into its own buffer (FP8) or stores straight from
 // the stage (BF16), releases the stage (empty[s]) once nothing reads it any
 // more, and bulk-stores the row to every destination.
-__host__ __device__ inline size_t scatter_head_bytes(int R) { return (static_cast<size_t>(R + 1) * 4 + 15) & ~15ull; }
+__host__ __device__ inline int scatter_head_ints(int mode, int R, int E) {
+  return mode == kSrcRanks ? R + 1 : mode == kSrcExpertMajor ? E + 1 : 0;
+}
+__host__ __device__ inline size_t scatter_head_bytes(int n) { return (static_cast<size_t>(n) * 4 + 15) & ~15ull; }
 __host__ __device__ inline size_t scatter_qbuf_bytes(int H) {
   return static_cast<size_t>(H) + ((4 * static_cast<size_t>(H / 128) + 15) & ~15ull);
 }
-__host__ __device__ inline size_t scatter_block_bytes(int H, int R, bool fp8, bool low_latency, int NS, int NC) {
-  return scatter_head_bytes(low_latency ? 0 : R) + 16 * static_cast<size_t>(NS) +
+__host__ __device__ inline size_t scatter_block_bytes(int H, int head_ints, bool fp8, int NS, int NC) {
+  return scatter_head_bytes(head_ints) + 16 * static_cast<size_t>(NS) +
          static_cast<size_t>(NS) * 2 * static_cast<size_t>(H) + (fp8 ? static_cast<size_t>(NC) * scatter_qbuf_bytes(H) : 0);
 }
 
-template <bool kFP8, bool kLL>
+template <bool kFP8, int kMode>
 __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_scatter(ScatterArgs a, int NS) {
+  constexpr bool kLL = kMode != kSrcRanks;  // per-entry destinations
+  constexpr bool kEM = kMode == kSrcExpertMajor;
   extern __shared__ __align__(128) unsigned char smem[];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -49,8 +59,8 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_scatter(
   const int H = a.H;
   const int G = H >> 7;
   const uint32_t row_bytes = 2u * static_cast<uint32_t>(H);
-  int* so = reinterpret_cast<int*>(smem);  // rank_offset (normal mode)
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + scatter_head_bytes(kLL ? 0 : a.R));
+  int* so = reinterpret_cast<int*>(smem);  // rank_offset (normal) / expert_offset (expert-major)
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + scatter_head_bytes(scatter_head_ints(kMode, a.R, a.E)));
   uint64_t* empty = full + NS;
   unsigned char* stage0 = reinterpret_cast<unsigned char*>(empty + NS);
   unsigned char* qbuf0 = stage0 + static_cast<size_t>(NS) * row_bytes;
@@ -58,6 +68,18 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_scatter(
 
   if (!kLL)
     for (int r = threadIdx.x; r <= a.R; r += blockDim.x) so[r] = a.rank_offset[r];
+  if (kEM) {
+    for (int e = threadIdx.x; e <= a.E; e += blockDim.x) so[e] = a.expert_offset[e];
+    // padding rows of the groups this block owns: no source token, weight 0
+    for (int e = blockIdx.x; e < a.E; e += gridDim.x) {
+      const long long end = min(static_cast<long long>(a.expert_offset[e + 1]), a.cap);
+      for (long long rw = static_cast<long long>(a.expert_offset[e]) + a.expert_count[e] + threadIdx.x; rw < end;
+           rw += blockDim.x) {
+        if (a.recv_src_idx) a.recv_src_idx[rw] = -1;
+        if (a.recv_weights) a.recv_weights[rw] = 0.0f;
+      }
+    }
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(full + s, 1);
@@ -114,7 +136,12 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_scatter(
     } else if (lane < a.k) {
       const int ee = a.ll_idx[static_cast<size_t>(t) * a.k + lane];
       const int ss = a.ll_slot[static_cast<size_t>(t) * a.k + lane];
-      if (ee >= 0 && ss >= 0) row = static_cast<long long>(ee) * a.M + ss;
+      if (ee >= 0 && ss >= 0) row = kEM ? static_cast<long long>(so[ee]) + ss : static_cast<long long>(ee) * a.M + ss;
+      if (kEM && row >= a.cap) {
+        latch_error(a.err, kErrCapacity);
+        row = -1;
+      }
+      if (kEM && row >= 0 && a.recv_weights) w = a.topk_weights[static_cast<size_t>(t) * a.k + lane];
     }
     const unsigned dmask = __ballot_sync(kFullMask, row >= 0);
     const bool landed = mbar_wait(full + s, static_cast<uint32_t>((i / NS) & 1), a.err);
@@ -135,7 +162,10 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_scatter(
         m &= m - 1;
         const long long rr = __shfl_sync(kFullMask, row, sl);
         if (lane == 0) bulk_store(static_cast<uint8_t*>(a.recv_x) + rr * H, qd, static_cast<uint32_t>(H));
-        for (int g = lane; g < G; g += 32) a.recv_scales[rr * G + g] = sd[g];
+        if (kEM)
+          for (int g = lane; g < G; g += 32) a.recv_scales[g * a.scales_ld + rr] = sd[g];
+        else
+          for (int g = lane; g < G; g += 32) a.recv_scales[rr * G + g] = sd[g];
       }
       if (lane == 0) bulk_commit();
     } else {
@@ -169,6 +199,9 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_scatter(
           if (a.recv_topk_weights) a.recv_topk_weights[rr * a.k + lane] = here ? w : 0.0f;
         }
       }
+    } else if (kEM && row >= 0) {
+      if (a.recv_src_idx) a.recv_src_idx[row] = t;
+      if (a.recv_weights) a.recv_weights[row] = w;
     } else if (kLL && a.recv_src_info && row >= 0) {
       a.recv_src_info[row] = t;
     }
@@ -180,11 +213,11 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_scatter(
 // Consumers and stages for a block: FP8 wants compute warps (8 consumers, the
 // rest of shared memory as stages); BF16 only moves bytes (4 consumers, more
 // stages).  Fewer consumers if the rows are long; 0 if not even two stages fit.
-void scatter_config(int H, int R, bool fp8, bool low_latency, size_t smem_limit, int* NS, int* NC) {
+void scatter_config(int H, int R, int E, bool fp8, int mode, size_t smem_limit, int* NS, int* NC) {
   *NS = 0;
   *NC = 0;
   for (int nc = fp8 ? kScatterMaxConsumers : 4; nc >= 1; --nc) {
-    const size_t fixed = scatter_block_bytes(H, R, fp8, low_latency, 0, nc);
+    const size_t fixed = scatter_block_bytes(H, scatter_head_ints(mode, R, E), fp8, 0, nc);
     if (fixed >= smem_limit) continue;
     const size_t per_stage = 16 + 2 * static_cast<size_t>(H);
     int ns = static_cast<int>((smem_limit - fixed) / per_stage);
@@ -197,15 +230,17 @@ void scatter_config(int H, int R, bool fp8, bool low_latency, size_t smem_limit,
   }
 }
 
-size_t scatter_smem_bytes(int H, int R, bool fp8, bool low_latency, int NS, int NC) {
-  return scatter_block_bytes(H, R, fp8, low_latency, NS, NC);
+size_t scatter_smem_bytes(int H, int R, int E, bool fp8, int mode, int NS, int NC) {
+  return scatter_block_bytes(H, scatter_head_ints(mode, R, E), fp8, NS, NC);
 }
 
 cudaError_t configure_scatter(size_t smem_limit) {
-  const void* ks[4] = {reinterpret_cast<const void*>(k_scatter<false, false>),
-                       reinterpret_cast<const void*>(k_scatter<true, false>),
-                       reinterpret_cast<const void*>(k_scatter<false, true>),
-                       reinterpret_cast<const void*>(k_scatter<true, true>)};
+  const void* ks[6] = {reinterpret_cast<const void*>(k_scatter<false, kSrcRanks>),
+                       reinterpret_cast<const void*>(k_scatter<true, kSrcRanks>),
+                       reinterpret_cast<const void*>(k_scatter<false, kSrcLowLatency>),
+                       reinterpret_cast<const void*>(k_scatter<true, kSrcLowLatency>),
+                       reinterpret_cast<const void*>(k_scatter<false, kSrcExpertMajor>),
+                       reinterpret_cast<const void*>(k_scatter<true, kSrcExpertMajor>)};
   for (const void* k : ks) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_limit));
     if (e != cudaSuccess) return e;
@@ -213,20 +248,24 @@ cudaError_t configure_scatter(size_t smem_limit) {
   return cudaSuccess;
 }
 
-void launch_scatter(const ScatterArgs& a, bool fp8, bool low_latency, int blocks, int NS, int NC,
-                    cudaStream_t stream) {
-  const size_t smem = scatter_block_bytes(a.H, a.R, fp8, low_latency, NS, NC);
+void launch_scatter(const ScatterArgs& a, bool fp8, int mode, int blocks, int NS, int NC, cudaStream_t stream) {
+  const size_t smem = scatter_block_bytes(a.H, scatter_head_ints(mode, a.R, a.E), fp8, NS, NC);
   const dim3 grid(blocks), block((NC + 1) * 32);
-  if (low_latency) {
+  if (mode == kSrcLowLatency) {
     if (fp8)
-      (void)launch_kernel(k_scatter<true, true>, grid, block, smem, stream, a, NS);
+      (void)launch_kernel(k_scatter<true, kSrcLowLatency>, grid, block, smem, stream, a, NS);
     else
-      (void)launch_kernel(k_scatter<false, true>, grid, block, smem, stream, a, NS);
+      (void)launch_kernel(k_scatter<false, kSrcLowLatency>, grid, block, smem, stream, a, NS);
+  } else if (mode == kSrcExpertMajor) {
+    if (fp8)
+      (void)launch_kernel(k_scatter<true, kSrcExpertMajor>, grid, block, smem, stream, a, NS);
+    else
+      (void)launch_kernel(k_scatter<false, kSrcExpertMajor>, grid, block, smem, stream, a, NS);
   } else {
     if (fp8)
-      (void)launch_kernel(k_scatter<true, false>, grid, block, smem, stream, a, NS);
+      (void)launch_kernel(k_scatter<true, kSrcRanks>, grid, block, smem, stream, a, NS);
     else
-      (void)launch_kernel(k_scatter<false, false>, grid, block, smem, stream, a, NS);
+      (void)launch_kernel(k_scatter<false, kSrcRanks>, grid, block, smem, stream, a, NS);
   }
 }
 

@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libep_gb300.so")
 
 EP_OK, EP_ERR_INVALID_ARG, EP_ERR_CUDA, EP_ERR_CAPACITY, EP_ERR_BAD_EXPERT, EP_ERR_TIMEOUT, EP_ERR_STATE = range(7)
 EP_BF16, EP_FP8_E4M3 = 0, 1
+EP_LAYOUT_RANK_MAJOR, EP_LAYOUT_LOW_LATENCY, EP_LAYOUT_EXPERT_MAJOR = 0, 1, 2
 
 _lock = threading.Lock()
 _lib = None
@@ -52,6 +53,11 @@ def lib() -> ctypes.CDLL:
             L.ep_handle_set_topk_idx_bits.argtypes = [P, I]
             L.ep_handle_topk_idx_bits.argtypes = [P]
             L.ep_handle_topk_idx_bits.restype = I
+            L.ep_em_layout_and_dispatch.argtypes = [P, P, I, P, P, I, I, P, P, I64, I64, P, P, I, P]
+            L.ep_em_dispatch.argtypes = [P, P, P, I, P, P, I64, I64, P, P, I, P]
+            L.ep_em_get_layout.argtypes = [P, P, P, P]
+            L.ep_em_combine.argtypes = [P, P, I64, P, I, P]
+            L.ep_get_buffer_size_hint.argtypes = [I, I, I, I, I, I, I, I, P, P]
             L.ep_layout_and_dispatch.argtypes = [P, P, I, P, P, I, P, P, I64, P, P, P, I, P]
             L.ep_low_latency_dispatch.argtypes = [P, P, P, I, I, P, P, P, P, I, P]
             L.ep_low_latency_combine.argtypes = [P, P, P, P, I, P]
@@ -62,6 +68,8 @@ def lib() -> ctypes.CDLL:
             for n in ("ep_handle_create", "ep_handle_destroy", "ep_get_dispatch_layout", "ep_get_num_recv",
                       "ep_dispatch", "ep_combine", "ep_layout_and_dispatch", "ep_low_latency_dispatch",
                       "ep_low_latency_combine", "ep_combine_ex", "ep_handle_set_topk_idx_bits",
+                      "ep_em_layout_and_dispatch", "ep_em_dispatch", "ep_em_get_layout", "ep_em_combine",
+                      "ep_get_buffer_size_hint",
                       "ep_get_device_status", "ep_get_dispatch_layout_noalloc"):
                 getattr(L, n).restype = I
             _lib = L
@@ -220,6 +228,60 @@ def ep_low_latency_combine(h, y, topk_weights, out, num_sms: int = 0, stream=Non
         _ptr(out, (torch.bfloat16,), "out"), int(num_sms), _stream(stream)), "ep_low_latency_combine")
 
 
+def _em_out(h, dtype, topk_weights, recv_x, recv_scales, recv_src_idx, recv_weights):
+    fp8 = dtype == EP_FP8_E4M3
+    cap = recv_x.shape[0] if recv_x is not None else 0
+    if fp8 and recv_scales is not None and (recv_scales.dim() != 2 or recv_scales.stride(1) != 1):
+        raise ValueError("recv_scales must be a contiguous [H/128, scales_ld] tensor")
+    ld = recv_scales.shape[1] if (fp8 and recv_scales is not None) else 0
+    return (_ptr(topk_weights, (torch.float32,), "topk_weights"), int(dtype),
+            _ptr(recv_x, _FP8_BYTES if fp8 else (torch.bfloat16,), "recv_x"),
+            _ptr(recv_scales, (torch.float32,), "recv_scales") if fp8 else None, ld, cap,
+            _ptr(recv_src_idx, (torch.int32,), "recv_src_idx"), _ptr(recv_weights, (torch.float32,), "recv_weights"))
+
+
+def ep_em_layout_and_dispatch(h, topk_idx, x, topk_weights, dtype: int, expert_alignment: int, recv_x,
+                              recv_scales=None, recv_src_idx=None, recv_weights=None, num_sms: int = 0,
+                              stream=None) -> None:
+    w, dt, rx, rs, ld, cap, si, rw = _em_out(h, dtype, topk_weights, recv_x, recv_scales, recv_src_idx, recv_weights)
+    _check(lib().ep_em_layout_and_dispatch(h, _ids_ptr(h, topk_idx), topk_idx.shape[0],
+                                           _ptr(x, (torch.bfloat16,), "x"), w, dt, int(expert_alignment), rx, rs,
+                                           ld, cap, si, rw, int(num_sms), _stream(stream)),
+           "ep_em_layout_and_dispatch")
+
+
+def ep_em_dispatch(h, x, topk_weights, dtype: int, recv_x, recv_scales=None, recv_src_idx=None, recv_weights=None,
+                   num_sms: int = 0, stream=None) -> None:
+    w, dt, rx, rs, ld, cap, si, rw = _em_out(h, dtype, topk_weights, recv_x, recv_scales, recv_src_idx, recv_weights)
+    _check(lib().ep_em_dispatch(h, _ptr(x, (torch.bfloat16,), "x"), w, dt, rx, rs, ld, cap, si, rw, int(num_sms),
+                                _stream(stream)), "ep_em_dispatch")
+
+
+def ep_em_get_layout(h, num_experts: int, stream=None, check: bool = True):
+    """-> (num_recv_tokens_per_expert [E], expert_offset [E+1]) numpy int32, status."""
+    a = np.zeros(num_experts, np.int32)
+    b = np.zeros(num_experts + 1, np.int32)
+    st = lib().ep_em_get_layout(h, a.ctypes.data, b.ctypes.data, _stream(stream))
+    if check:
+        _check(st, "ep_em_get_layout")
+    return a, b, st
+
+
+def ep_em_combine(h, y, out, num_sms: int = 0, stream=None) -> None:
+    _check(lib().ep_em_combine(h, _ptr(y, (torch.bfloat16,), "y"), y.shape[0], _ptr(out, (torch.bfloat16,), "out"),
+                               int(num_sms), _stream(stream)), "ep_em_combine")
+
+
+def ep_get_buffer_size_hint(num_ranks, num_experts, num_topk, hidden, max_tokens_per_rank, dtype: int,
+                            layout: int, expert_alignment: int = 1):
+    """-> (rows, bytes): the largest receive buffers any routing can need."""
+    rows, nbytes = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().ep_get_buffer_size_hint(num_ranks, num_experts, num_topk, hidden, max_tokens_per_rank, int(dtype),
+                                         int(layout), int(expert_alignment), ctypes.byref(rows),
+                                         ctypes.byref(nbytes)), "ep_get_buffer_size_hint")
+    return rows.value, nbytes.value
+
+
 def ep_get_device_status(h, stream=None) -> int:
     """Synchronise, then return and clear the latched device status."""
     return lib().ep_get_device_status(h, _stream(stream))
@@ -263,6 +325,7 @@ class Handle:
         self.max_tokens_per_rank = max_tokens_per_rank
         self.T = None      # tokens of the last layout
         self.T_ll = None   # tokens of the last low-latency dispatch
+        self.T_em = None   # tokens of the last expert-major layout
         self.ptr = ep_handle_create(num_ranks, num_experts, num_topk, hidden, max_tokens_per_rank)
 
     @property
@@ -406,6 +469,52 @@ class Handle:
         self._need(topk_weights, self.T_ll * self.k, "topk_weights")
         self._need(out, self.T_ll * self.H, "out")
         ep_low_latency_combine(self.ptr, y, topk_weights, out, num_sms, stream)
+
+    # -------------------------------------------------------- expert-major
+
+    def _em_need(self, T, topk_weights, dtype, recv_x, recv_scales, recv_src_idx, recv_weights):
+        if recv_x.dim() != 2 or recv_x.shape[1] != self.H:
+            raise ValueError(f"recv_x must be [cap, {self.H}]")
+        cap = recv_x.shape[0]
+        self._need(topk_weights, T * self.k, "topk_weights")
+        if dtype == EP_FP8_E4M3:
+            if recv_scales is None or recv_scales.dim() != 2 or recv_scales.shape[0] != self.G:
+                raise ValueError(f"FP8 dispatch needs recv_scales [{self.G}, scales_ld]")
+            if recv_scales.shape[1] < cap:
+                raise ValueError("scales_ld must be >= the capacity rows")
+        self._need(recv_src_idx, cap, "recv_src_idx")
+        self._need(recv_weights, cap, "recv_weights")
+
+    def em_layout_and_dispatch(self, topk_idx, x, topk_weights, dtype, expert_alignment, recv_x, recv_scales=None,
+                               recv_src_idx=None, recv_weights=None, num_sms=0, stream=None):
+        T = topk_idx.shape[0]
+        if topk_idx.dim() != 2 or topk_idx.shape[1] != self.k:
+            raise ValueError(f"topk_idx must be [T, {self.k}]")
+        self._need(x, T * self.H, "x")
+        self._em_need(T, topk_weights, dtype, recv_x, recv_scales, recv_src_idx, recv_weights)
+        ep_em_layout_and_dispatch(self.ptr, topk_idx, x, topk_weights, dtype, expert_alignment, recv_x, recv_scales,
+                                  recv_src_idx, recv_weights, num_sms, stream)
+        self.T_em = T
+
+    def em_dispatch(self, x, topk_weights, dtype, recv_x, recv_scales=None, recv_src_idx=None, recv_weights=None,
+                    num_sms=0, stream=None):
+        if self.T_em is None:
+            raise RuntimeError("expert-major dispatch before any expert-major layout")
+        self._need(x, self.T_em * self.H, "x")
+        self._em_need(self.T_em, topk_weights, dtype, recv_x, recv_scales, recv_src_idx, recv_weights)
+        ep_em_dispatch(self.ptr, x, topk_weights, dtype, recv_x, recv_scales, recv_src_idx, recv_weights, num_sms,
+                       stream)
+
+    def em_get_layout(self, stream=None, check=True):
+        return ep_em_get_layout(self.ptr, self.E, stream=stream, check=check)
+
+    def em_combine(self, y, out, num_sms=0, stream=None):
+        if self.T_em is None:
+            raise RuntimeError("expert-major combine before any expert-major layout")
+        if y.dim() != 2 or y.shape[1] != self.H:
+            raise ValueError(f"y must be [rows, {self.H}]")
+        self._need(out, self.T_em * self.H, "out")
+        ep_em_combine(self.ptr, y, out, num_sms, stream)
 
     def get_device_status(self, stream=None):
         return ep_get_device_status(self.ptr, stream)

@@ -75,6 +75,12 @@ typedef enum {
 
 typedef enum { EP_BF16 = 0, EP_FP8_E4M3 = 1 } ep_dtype_t;
 
+/* Receive layouts: rank-major (ep_dispatch: one row per (token,
+ * destination rank), ranks' regions packed), low latency ([E][M][H] per
+ * expert), expert-major (ep_em_*: one row per (token, expert) entry, expert
+ * groups packed and aligned). */
+typedef enum { EP_LAYOUT_RANK_MAJOR = 0, EP_LAYOUT_LOW_LATENCY = 1, EP_LAYOUT_EXPERT_MAJOR = 2 } ep_layout_t;
+
 /* Create a handle for R ranks, E experts (E % R == 0), top-k = num_topk
  * (1..32), hidden size H (multiple of 128) and at most max_tokens_per_rank
  * tokens per source rank (so T <= R * max_tokens_per_rank).  Allocates, once,
@@ -248,6 +254,83 @@ ep_status_t ep_low_latency_dispatch(ep_handle_t h, const void* x, const void* to
  *                   ties), from +0.0, rounded to bf16 (nearest-even). */
 ep_status_t ep_low_latency_combine(ep_handle_t h, const void* y, const float* topk_weights,
                                    void* out, int num_sms, ep_stream_t stream);
+
+/* ---------------------------------------------------------------------
+ * Expert-major ("GEMM") receive layout -- the "new GEMM layout" of the V2
+ * release ("DeepSeek công bố thư viện mã nguồn mở DeepEP ..." (vi.news.hada.io),
+ * "Những thay đổi chính của bản phát hành V2"), read as: the rows a grouped
+ * GEMM consumes directly, one row per unmasked (token, k) entry, grouped by
+ * expert in ascending expert id (so rank r's experts form one contiguous
+ * region), the entries of one expert in (source rank, token, k-index) order,
+ * and each expert's group starting at a multiple of `expert_alignment` rows
+ * (the GEMM's M tile).  Padding rows carry source -1 and weight 0; their
+ * payload and scales are not written.  FP8 scales are stored group-major,
+ * scales[g * scales_ld + row], so the scales of one 128-channel group of
+ * consecutive rows are contiguous (scales_ld >= capacity rows, a multiple of
+ * 4 so every group's column starts 16-byte aligned).
+ * --------------------------------------------------------------------- */
+
+/* Expert-major layout and dispatch in one call.
+ * In:  topk_idx [T][k] (width per ep_handle_set_topk_idx_bits), x bf16 [T][H],
+ *      topk_weights fp32 [T][k] or NULL, dtype, expert_alignment (1..65536;
+ *      T*k + E*(alignment-1) must fit in int32).
+ * Out: recv_x [cap][H] (e4m3 bytes or bf16); recv_scales fp32
+ *      [H/128][scales_ld] (FP8 only); recv_src_idx int32 [cap] or NULL (the
+ *      row's source token, -1 on padding); recv_weights fp32 [cap] or NULL
+ *      (needs topk_weights; the entry's weight, 0 on padding).
+ *      Rows at or past recv_capacity_rows are skipped and latch
+ *      EP_ERR_CAPACITY; at most T*k + E*(alignment-1) rows are needed.
+ * The handle keeps the layout for ep_em_get_layout, ep_em_dispatch and
+ * ep_em_combine.  Usually one cooperative launch (as ep_layout_and_dispatch);
+ * with more than 4096 (token, k) entries per SM a routing kernel, a one-block
+ * offsets kernel and the row scatter.  H must leave room for two staged rows
+ * in shared memory (H <= ~50k), else EP_ERR_INVALID_ARG. */
+ep_status_t ep_em_layout_and_dispatch(ep_handle_t h, const void* topk_idx, int num_tokens, const void* x,
+                                      const float* topk_weights, ep_dtype_t dtype, int expert_alignment,
+                                      void* recv_x, float* recv_scales, int64_t scales_ld,
+                                      int64_t recv_capacity_rows, int* recv_src_idx, float* recv_weights,
+                                      int num_sms, ep_stream_t stream);
+
+/* Dispatch another tensor (e.g. gradients, "DeepEP 要約" section 3: the
+ * backward of combine is dispatch) through the handle's last expert-major
+ * layout; arguments as ep_em_layout_and_dispatch. */
+ep_status_t ep_em_dispatch(ep_handle_t h, const void* x, const float* topk_weights, ep_dtype_t dtype,
+                           void* recv_x, float* recv_scales, int64_t scales_ld, int64_t recv_capacity_rows,
+                           int* recv_src_idx, float* recv_weights, int num_sms, ep_stream_t stream);
+
+/* Copy the last expert-major layout to host memory; synchronises `stream`.
+ * Out (each may be NULL): num_recv_tokens_per_expert host int32 [E] (rows
+ * per expert, without padding: the grouped GEMM's per-expert M),
+ * expert_offset host int32 [E+1] (first row of each group; [E] = rows
+ * used).  Returns the latched device status, if any (without clearing it). */
+ep_status_t ep_em_get_layout(ep_handle_t h, int* num_recv_tokens_per_expert, int* expert_offset,
+                             ep_stream_t stream);
+
+/* Expert-major combine: out bf16 [T][H] = for each token, the fp32 sum of
+ * its rows of y (bf16 [y_rows][H], laid out like ep_em_* recv_x) over its
+ * unmasked entries in ascending expert id (k-index breaks ties), from +0.0,
+ * rounded to bf16 (nearest-even); unweighted, as ep_combine (the entry's
+ * weight is the expert side's to apply, e.g. in the GEMM epilogue, from
+ * recv_weights).  Rows at or past y_rows are skipped and latch
+ * EP_ERR_CAPACITY. */
+ep_status_t ep_em_combine(ep_handle_t h, const void* y, int64_t y_rows, void* out, int num_sms,
+                          ep_stream_t stream);
+
+/* Receive-buffer sizes for a configuration, before any routing is known
+ * (the pages' get_buffer_size_hint: the size needed, to allocate once or to
+ * check that an existing buffer can be reused; vi.news.hada.io, "Giao diện
+ * xoay quanh ElasticBuffer").  Needs no GPU and no handle.
+ * Out: *rows   the most receive rows any routing can need: T*min(k,R)
+ *              (rank-major), E*M (low latency, M = R*max_tokens_per_rank),
+ *              T*k + E*(alignment-1) (expert-major), T = R*max_tokens_per_rank;
+ *      *bytes  the bytes of all receive-side buffers at that row count:
+ *              payload (+ fp32 scales for FP8), plus per row the source
+ *              index and (rank-major) k local ids and k weights, (low
+ *              latency) plus E counts, (expert-major) one weight, with
+ *              scales_ld = rows rounded up to 4. */
+ep_status_t ep_get_buffer_size_hint(int num_ranks, int num_experts, int num_topk, int hidden,
+                                    int max_tokens_per_rank, ep_dtype_t dtype, ep_layout_t layout,
+                                    int expert_alignment, int64_t* rows, int64_t* bytes);
 
 /* ep_get_dispatch_layout_noalloc -- the same layout computation as
  * ep_get_dispatch_layout, for callers that cannot allocate device memory.
