@@ -52,7 +52,7 @@ struct ep_handle {
   int* em_count;
   int* em_offset;
   int* fused_agg;               // [num_sms][R+E] per-block counts of the fused kernel
-  unsigned* fused_barrier;      // [2] its grid barrier words
+  unsigned* fused_barrier;      // [4 + num_sms] its control words (barrier, row claims, published flags)
   size_t smem_optin;
   int* err;
   // pinned host mirror: err, then R + E + R+1 counts
@@ -247,7 +247,7 @@ ep_status_t ep_handle_create(int R, int E, int k, int H, int max_tpr, ep_handle_
   const size_t o_emcnt = take(sizeof(int) * E);
   const size_t o_emoff = take(sizeof(int) * (E + 1));
   const size_t o_fagg = take(sizeof(int) * static_cast<size_t>(h->num_sms) * (R + E));
-  const size_t o_fbar = take(sizeof(unsigned) * 2);
+  const size_t o_fbar = take(sizeof(unsigned) * (4 + static_cast<size_t>(h->num_sms)));
   const size_t o_err = take(sizeof(int));
   if ((st = cuda_status(cudaMalloc(&h->arena, off), "cudaMalloc")) != EP_OK) {
     delete h;
@@ -921,6 +921,12 @@ ep_status_t ep_get_device_status(ep_handle_t h, ep_stream_t stream) {
   if (e == cudaSuccess) e = cudaMemsetAsync(h->err, 0, sizeof(int), s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if ((st = cuda_status(e, "ep_get_device_status")) != EP_OK) return st;
+  if (h->host[0] == EP_ERR_TIMEOUT) {
+    // a wait gave up somewhere: start the fused kernel's control words afresh
+    e = cudaMemsetAsync(h->fused_barrier, 0, sizeof(unsigned) * (4 + static_cast<size_t>(h->num_sms)), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if ((st = cuda_status(e, "ep_get_device_status reset")) != EP_OK) return st;
+  }
   return static_cast<ep_status_t>(h->host[0]);
 }
 

@@ -15,10 +15,15 @@
 //                   counts in shared memory.
 // Each block publishes its counts, all blocks meet at one bounded grid
 // barrier (co-residency guaranteed by the cooperative launch), and each block
-// sums its predecessors' counts into exclusive prefixes.  The destination
-// rows are then known and the consumer warps quantise / store the rows
-// exactly as k_scatter does; per-expert totals, which nothing waits for, are
-// formed after the rows.  Rows and slots come out identical to the separate
+// sums its predecessors' counts into exclusive prefixes, writes its tokens'
+// destinations and publishes them.  The row movement is not tied to the
+// routing's token ranges: the producer warps claim tokens in pairs from one
+// global counter from the first instruction on, so an SM that moves rows
+// faster takes more of them (the SMs of one GB300 do not all stream at the
+// same rate); a consumer reads a claimed token's destinations from global
+// memory once the owning block has published them, then quantises / stores
+// the row exactly as k_scatter does.  Per-expert totals, which nothing waits
+// for, are formed after the rows.  Rows and slots come out identical to the separate
 // routing kernels: (source rank, token) order per rank, (source rank, token,
 // k) order per expert.  The expert-major ("GEMM") layout of the V2 release
 // notes in "DeepSeek công bố thư viện mã nguồn mở DeepEP ..."
@@ -50,6 +55,12 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
 __device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" : : "l"(p), "r"(v) : "memory");
 }
+
+// Control words (FusedArgs::barrier): [0] barrier arrivals, [1] barrier
+// generation, [2] row-claim counter, [3] blocks finished, [4 + b] block b's
+// "destinations published" word (= generation + 1 once written).
+constexpr int kCtlClaim = 2, kCtlDone = 3, kCtlPub = 4;
+constexpr int kClaimTokens = 2;  // tokens per claim
 
 // Grid-wide barrier among the consumer warps of all blocks.  Word 0 counts
 // arrivals, word 1 is the generation, which thread 32 read (into g) when the
@@ -151,7 +162,6 @@ __device__ inline void column_sums_par(const int* agg, int NK, int ncols, int nb
 __host__ __device__ inline size_t fused_route_bytes(int mode, int R, int E, int kmax, int kp, int tpb, int nc) {
   if (mode == kSrcRanks)
     return 8 * static_cast<size_t>(tpb)                        // token rank masks (u64)
-           + 8 * static_cast<size_t>(tpb) * kmax               // (rank, row) per token
            + 4 * static_cast<size_t>(tpb) * kmax               // local rows
            + 4 * (static_cast<size_t>(nc) * R + E + 3 * (R + 1) + 4);
   const size_t ni = static_cast<size_t>(tpb) * kp;
@@ -187,7 +197,8 @@ __host__ __device__ inline size_t fused_smem_bytes(int mode, bool fp8, int R, in
                                                    int nc, int ns, int H) {
   const size_t route = (fused_route_bytes(mode, R, E, kmax, kp, tpb, nc) + 127) & ~static_cast<size_t>(127);
   const size_t qb = static_cast<size_t>(H) + ((4 * static_cast<size_t>(H / 128) + 15) & ~15ull);
-  return route + 16 * static_cast<size_t>(ns) + static_cast<size_t>(ns) * 2 * H + (fp8 ? nc * qb : 0);
+  return route + 16 * static_cast<size_t>(ns) + ((4 * static_cast<size_t>(ns) + 4 + 15) & ~15ull) +
+         static_cast<size_t>(ns) * 2 * H + (fp8 ? nc * qb : 0);
 }
 
 template <bool kFP8, int kMode>
@@ -213,14 +224,11 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
   // ---- shared memory carve-up
   unsigned char* p = smem;
   unsigned long long* tmask = nullptr;
-  int2* tdst = nullptr;
   int *tlocal = nullptr, *cnt = nullptr, *hist = nullptr, *so = nullptr, *excl = nullptr, *tot = nullptr;
   int *item_e = nullptr, *item_slot = nullptr, *etot = nullptr, *eoff = nullptr, *wsum = nullptr;
   if (!kLL) {
     tmask = reinterpret_cast<unsigned long long*>(p);
     p += 8 * static_cast<size_t>(tpb);
-    tdst = reinterpret_cast<int2*>(p);
-    p += 8 * static_cast<size_t>(tpb) * kmax;
     tlocal = reinterpret_cast<int*>(p);
     p += 4 * static_cast<size_t>(tpb) * kmax;
     cnt = reinterpret_cast<int*>(p);   // [NC][R]
@@ -242,7 +250,9 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
   unsigned char* sbase = smem + ((fused_route_bytes(kMode, R, E, kmax, kp, tpb, NC) + 127) & ~static_cast<size_t>(127));
   uint64_t* full = reinterpret_cast<uint64_t*>(sbase);
   uint64_t* empty = full + NS;
-  unsigned char* stage0 = reinterpret_cast<unsigned char*>(empty + NS);
+  int* stage_tok = reinterpret_cast<int*>(empty + NS);  // token held by each stage (-1: no more)
+  unsigned* sh_gen = reinterpret_cast<unsigned*>(stage_tok + NS);
+  unsigned char* stage0 = reinterpret_cast<unsigned char*>(stage_tok) + ((4 * NS + 4 + 15) & ~15);
   unsigned char* qbuf0 = stage0 + static_cast<size_t>(NS) * row_bytes;
   auto stage = [&](int s) { return stage0 + static_cast<size_t>(s) * row_bytes; };
 
@@ -252,27 +262,48 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
       mbar_init(empty + s, 1);
     }
     mbar_init_fence();
+    // the grid barrier's generation: written last by the previous launch (a
+    // relaxed load sees it), and it cannot change before this block arrives
+    *sh_gen = ld_relaxed_u32(a.barrier + 1);
   }
   __syncthreads();
+  const unsigned gen = *sh_gen;
 
   if (warp == 0) {
-    // producer: the block's rows, in order, from the first instruction on
+    // producer: claims tokens kClaimTokens at a time (one claim ahead) and
+    // streams their rows into the stages from the first instruction on; when
+    // the claims run out it hands every consumer warp a "no more" stage
     if (lane == 0) {
-      for (int i = 0; i < n_own; ++i) {
-        const int s = i % NS;
-        if (i >= NS && !mbar_wait(empty + s, static_cast<uint32_t>((i / NS - 1) & 1), a.err)) break;
-        mbar_arrive_expect_tx(full + s, row_bytes);
-        bulk_load(stage(s), a.x + static_cast<size_t>(t_begin + i) * H, row_bytes, full + s);
+      unsigned* claim = a.barrier + kCtlClaim;
+      int base = static_cast<int>(atomicAdd(claim, static_cast<unsigned>(kClaimTokens)));
+      int next = base < a.T ? static_cast<int>(atomicAdd(claim, static_cast<unsigned>(kClaimTokens))) : a.T;
+      int i = 0;
+      bool ok = true;
+      while (ok && base < a.T) {
+        for (int c = 0; c < kClaimTokens && base + c < a.T; ++c, ++i) {
+          const int s = i % NS;
+          if (i >= NS && !mbar_wait(empty + s, static_cast<uint32_t>((i / NS - 1) & 1), a.err)) {
+            ok = false;
+            break;
+          }
+          stage_tok[s] = base + c;
+          mbar_arrive_expect_tx(full + s, row_bytes);
+          bulk_load(stage(s), a.x + static_cast<size_t>(base + c) * H, row_bytes, full + s);
+        }
+        base = next;
+        if (base < a.T) next = static_cast<int>(atomicAdd(claim, static_cast<unsigned>(kClaimTokens)));
+      }
+      for (int j = i; ok && j < i + NC; ++j) {
+        const int s = j % NS;
+        if (j >= NS && !mbar_wait(empty + s, static_cast<uint32_t>((j / NS - 1) & 1), a.err)) break;
+        stage_tok[s] = -1;
+        mbar_arrive(full + s);
       }
     }
     return;
   }
 
   const int cw = warp - 1;  // consumer warp
-  // the grid barrier's generation: written last by the previous launch, so a
-  // relaxed load sees it (and, unlike an acquire, does not hold back the loads
-  // that follow)
-  const unsigned gen = threadIdx.x == 32 ? ld_relaxed_u32(a.barrier + 1) : 0u;
   const unsigned lt = lanemask_lt();
   // ---------------------------------------------------------------- phase 1: rank the block's tokens
   if (!kLL) {
@@ -428,13 +459,9 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
         m &= m - 1;
         const int in_rank = excl[r] + cnt[w * R + r] + tlocal[tl * kmax + pos];
         a.dst[static_cast<size_t>(t) * kmax + pos] = make_int2(r, in_rank);
-        tdst[tl * kmax + pos] = make_int2(r, so[r] + in_rank);
         ++pos;
       }
-      for (; pos < kmax; ++pos) {
-        a.dst[static_cast<size_t>(t) * kmax + pos] = make_int2(-1, -1);
-        tdst[tl * kmax + pos] = make_int2(-1, -1);
-      }
+      for (; pos < kmax; ++pos) a.dst[static_cast<size_t>(t) * kmax + pos] = make_int2(-1, -1);
     }
   } else {
     column_sums_par(a.agg, NK, E, nb, b, excl, kEM ? etot : nullptr, nct, ct);
@@ -472,32 +499,57 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
       }
       a.ll_idx[static_cast<size_t>(t) * k + j] = e;
       a.ll_slot[static_cast<size_t>(t) * k + j] = slot;
-      if (kEM && slot >= 0 && static_cast<long long>(eoff[e]) + slot >= a.cap) {
-        latch_error(a.err, kErrCapacity);  // the row does not fit the receive buffer
-        slot = -1;
-      }
-      item_slot[i] = slot;
     }
   }
   consumer_sync(nct);
+  if (threadIdx.x == 32) {  // this block's destinations are visible to every block
+    __threadfence();
+    st_release_u32(a.barrier + kCtlPub + b, gen + 1);
+  }
 
   // ---------------------------------------------------------------- phase 3: move the rows
   unsigned char* qd = qbuf0 + static_cast<size_t>(cw) * (static_cast<size_t>(H) + ((4 * G + 15) & ~15));
   float* sd = reinterpret_cast<float*>(qd + H);
   const bool meta = !kLL && (a.recv_src_idx || a.recv_topk_idx || a.recv_topk_weights);
   bool first = true;
-  for (int i = cw; i < n_own; i += NC) {
-    const int t = t_begin + i;
+  int owner_ok = b;  // the owning block whose destinations were last seen published
+  for (int i = cw;; i += NC) {
     const int s = i % NS;
+    const bool landed = mbar_wait(full + s, static_cast<uint32_t>((i / NS) & 1), a.err);
+    if (!__all_sync(kFullMask, landed)) break;
+    const int t = stage_tok[s];
+    if (t < 0) {  // no more rows
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + s);
+      break;
+    }
+    // the owning block's destinations: published words, then plain L2 loads
+    const int owner = t / tpb;
+    bool have = true;
+    if (owner != owner_ok) {
+      int it = 0;
+      while (ld_acquire_u32(a.barrier + kCtlPub + owner) != gen + 1) {
+        if (++it > kSpinLimit) {
+          latch_error(a.err, kErrTimeout);
+          have = false;
+          break;
+        }
+        if (it > 16) __nanosleep(64);
+      }
+      have = __all_sync(kFullMask, have);
+      if (have) owner_ok = owner;
+    }
     long long row = -1;
     int r = -1, e = -1;
     float w = 0.0f;
-    if (!kLL) {
+    if (!have) {
+      // gave up waiting (latched): the token's rows are skipped
+    } else if (!kLL) {
       if (lane < kmax) {
-        const int2 d = tdst[i * kmax + lane];
+        const int2 d = __ldcg(a.dst + static_cast<size_t>(t) * kmax + lane);
         if (d.x >= 0) {
           r = d.x;
-          row = d.y;
+          row = static_cast<long long>(so[d.x]) + d.y;
           if (row >= a.cap) {
             latch_error(a.err, kErrCapacity);
             row = -1;
@@ -505,18 +557,20 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
         }
       }
       if (meta && lane < k) {
-        e = a.idx32[static_cast<size_t>(t) * k + lane];
+        e = __ldcg(a.idx32 + static_cast<size_t>(t) * k + lane);
         if (a.topk_weights) w = a.topk_weights[static_cast<size_t>(t) * k + lane];
       }
     } else if (lane < k) {
-      const int ee = item_e[(i << a.kp_log2) + lane];
-      const int sl = item_slot[(i << a.kp_log2) + lane];
+      const int ee = __ldcg(a.ll_idx + static_cast<size_t>(t) * k + lane);
+      const int sl = __ldcg(a.ll_slot + static_cast<size_t>(t) * k + lane);
       if (ee >= 0 && sl >= 0) row = kEM ? static_cast<long long>(eoff[ee]) + sl : static_cast<long long>(ee) * a.M + sl;
+      if (kEM && row >= a.cap) {
+        latch_error(a.err, kErrCapacity);  // the row does not fit the receive buffer
+        row = -1;
+      }
       if (kEM && row >= 0 && a.recv_weights) w = a.topk_weights[static_cast<size_t>(t) * k + lane];
     }
     const unsigned dmask = __ballot_sync(kFullMask, row >= 0);
-    const bool landed = mbar_wait(full + s, static_cast<uint32_t>((i / NS) & 1), a.err);
-    if (!__all_sync(kFullMask, landed)) break;
     if (kFP8) {
       if (!first) {
         if (lane == 0) bulk_wait_read<0>();
@@ -604,6 +658,13 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
   }
   if (lane == 0) bulk_wait_all();
   __syncwarp();
+  // the last block to finish resets the claim counter for the next launch
+  // (every claim of every block has returned by the time it counts itself)
+  consumer_sync(nct);
+  if (threadIdx.x == 32 && atomicAdd(a.barrier + kCtlDone, 1u) == static_cast<unsigned>(nb) - 1) {
+    atomicExch(a.barrier + kCtlClaim, 0u);
+    atomicExch(a.barrier + kCtlDone, 0u);
+  }
 }
 
 // Blocks, stages and consumers for the fused kernel; blocks = 0 when it does
@@ -621,8 +682,9 @@ void fused_config(int mode, bool fp8, int T, int R, int E, int k, int kmax, int 
   for (int nc = fp8 ? kScatterMaxConsumers : 4; nc >= 1; --nc) {
     const size_t fixed = fused_smem_bytes(mode, fp8, R, E, kmax, kp, tpb, nc, 0, H);
     if (fixed >= smem_limit) continue;
-    int ns = static_cast<int>((smem_limit - fixed) / (16 + 2 * static_cast<size_t>(H)));
+    int ns = static_cast<int>((smem_limit - fixed) / (20 + 2 * static_cast<size_t>(H)));
     if (ns > 32) ns = 32;
+    while (ns >= 2 && fused_smem_bytes(mode, fp8, R, E, kmax, kp, tpb, nc, ns, H) > smem_limit) --ns;
     if (ns >= 2) {
       *blocks = nb;
       *NS = ns;

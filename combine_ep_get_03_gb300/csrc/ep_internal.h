@@ -143,7 +143,7 @@ struct FusedArgs {
   const float* topk_weights;
   int T, R, E, El, k, kp_log2, kmax, H, M;
   int* agg;           // [blocks][R+E] (normal) or [blocks][E] (low latency)
-  unsigned* barrier;  // [2] grid barrier words
+  unsigned* barrier;  // [4 + blocks] control words: grid barrier, row claims, published flags
   int* err;
   // normal mode: the handle's layout state and the dispatch outputs
   int2* dst;
