@@ -434,6 +434,7 @@ ep_status_t ep_dispatch(ep_handle_t h, const void* x, const float* topk_weights,
     a.recv_topk_weights = recv_topk_weights;
     a.recv_x = recv_x;
     a.recv_scales = recv_scales;
+    a.ctl = h->fused_barrier;
     a.err = h->err;
     const int blocks = grid_for(h, 1, num_sms, T, 1);
     ep::launch_scatter(a, fp8, ep::kSrcRanks, blocks, sns, snc, reinterpret_cast<cudaStream_t>(stream));
@@ -625,6 +626,7 @@ ep_status_t ep_low_latency_dispatch(ep_handle_t h, const void* x, const void* to
     a.recv_src_info = recv_src_info;
     a.recv_x = recv_x;
     a.recv_scales = recv_scales;
+    a.ctl = h->fused_barrier;
     a.err = h->err;
     const int blocks = grid_for(h, 1, num_sms, T, 1);
     ep::launch_scatter(a, fp8, ep::kSrcLowLatency, blocks, sns, snc, s);
@@ -730,6 +732,7 @@ ep_status_t em_scatter(ep_handle* h, const void* x, const float* topk_weights, b
   a.scales_ld = scales_ld;
   a.recv_x = recv_x;
   a.recv_scales = recv_scales;
+  a.ctl = h->fused_barrier;
   a.err = h->err;
   const int sns = h->scatter_ns[fp8 ? 1 : 0][ep::kSrcExpertMajor], snc = h->scatter_nc[fp8 ? 1 : 0][ep::kSrcExpertMajor];
   const int blocks = grid_for(h, 1, num_sms, T, 1);

@@ -38,10 +38,6 @@
 
 namespace ep {
 
-__device__ __forceinline__ void consumer_sync(int nthreads) {
-  asm volatile("bar.sync 1, %0;" : : "r"(nthreads) : "memory");
-}
-
 __device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
   unsigned v;
   asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -55,12 +51,6 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
 __device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" : : "l"(p), "r"(v) : "memory");
 }
-
-// Control words (FusedArgs::barrier): [0] barrier arrivals, [1] barrier
-// generation, [2] row-claim counter, [3] blocks finished, [4 + b] block b's
-// "destinations published" word (= generation + 1 once written).
-constexpr int kCtlClaim = 2, kCtlDone = 3, kCtlPub = 4;
-constexpr int kClaimTokens = 2;  // tokens per claim
 
 // Grid-wide barrier among the consumer warps of all blocks.  Word 0 counts
 // arrivals, word 1 is the generation, which thread 32 read (into g) when the
@@ -518,7 +508,8 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
     const bool landed = mbar_wait(full + s, static_cast<uint32_t>((i / NS) & 1), a.err);
     if (!__all_sync(kFullMask, landed)) break;
     const int t = stage_tok[s];
-    if (t < 0) {  // no more rows
+    if (t >= a.T) latch_error(a.err, kErrState);  // never written by the producer: cannot happen
+    if (t < 0 || t >= a.T) {  // no more rows
       __syncwarp();
       if (lane == 0) mbar_arrive(empty + s);
       break;
@@ -679,19 +670,23 @@ void fused_config(int mode, bool fp8, int T, int R, int E, int k, int kmax, int 
   const int nb = sms;
   const int tpb = fused_tokens_per_block(T, nb);
   if (tpb * kp > kFusedMaxItems) return;
-  for (int nc = fp8 ? kScatterMaxConsumers : 4; nc >= 1; --nc) {
-    const size_t fixed = fused_smem_bytes(mode, fp8, R, E, kmax, kp, tpb, nc, 0, H);
-    if (fixed >= smem_limit) continue;
-    int ns = static_cast<int>((smem_limit - fixed) / (20 + 2 * static_cast<size_t>(H)));
-    if (ns > 32) ns = 32;
-    while (ns >= 2 && fused_smem_bytes(mode, fp8, R, E, kmax, kp, tpb, nc, ns, H) > smem_limit) --ns;
-    if (ns >= 2) {
-      *blocks = nb;
-      *NS = ns;
-      *NC = nc;
-      return;
+  const int max_nc = fp8 ? kScatterMaxConsumers : 4;
+  for (int pass = 0; pass < 2 && *NS == 0; ++pass) {
+    // first at least half the consumers (the quantiser's compute), then any
+    for (int nc = max_nc; nc >= (pass == 0 ? (max_nc + 1) / 2 : 1); --nc) {
+      const size_t fixed = fused_smem_bytes(mode, fp8, R, E, kmax, kp, tpb, nc, 0, H);
+      if (fixed >= smem_limit) continue;
+      int ns = static_cast<int>((smem_limit - fixed) / (20 + 2 * static_cast<size_t>(H)));
+      if (ns > 32) ns = 32;
+      while (ns >= 2 && fused_smem_bytes(mode, fp8, R, E, kmax, kp, tpb, nc, ns, H) > smem_limit) --ns;
+      ns -= ns % nc;  // consumer c owns the stages s = c (mod nc), as in k_scatter
+      if (ns >= 2 && ns >= nc && ns > *NS) {  // the most stages; more consumers on a tie
+        *NS = ns;
+        *NC = nc;
+      }
     }
   }
+  if (*NS > 0) *blocks = nb;
 }
 
 cudaError_t configure_fused(size_t smem_limit) {

@@ -96,6 +96,14 @@ size_t combine_smem_bytes(int src, int R, int E);
 int combine_threads();
 const void* combine_kernel(int src, bool fp8);
 
+// Control words shared by the row-moving kernels (the handle's
+// fused_barrier array): [0] grid-barrier arrivals, [1] grid-barrier
+// generation, [2] row-claim counter, [3] blocks finished (the last block
+// resets [2] and [3]), [4 + b] block b's "destinations published" word of
+// the fused kernel (= generation + 1 once written).
+constexpr int kCtlClaim = 2, kCtlDone = 3, kCtlPub = 4;
+constexpr int kClaimTokens = 2;  // tokens per claim
+
 // TMA bulk-copy scatter (dispatch row movement), persistent: one block per
 // SM, one producer warp and up to kScatterMaxConsumers consumer warps.
 constexpr int kScatterMaxConsumers = 8;
@@ -125,6 +133,7 @@ struct ScatterArgs {
   // outputs
   void* recv_x;
   float* recv_scales;
+  unsigned* ctl;               // control words (row claims)
   int* err;
 };
 // NS row stages and NC consumer warps that fit `smem_limit` (NS = 0: the

@@ -6,6 +6,12 @@
 
 namespace ep {
 
+// Named barrier 1 among the consumer warps (warps 1..NC) of a block.
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+  asm volatile("bar.sync 1, %0;" : : "r"(nthreads) : "memory");
+}
+
+
 // Largest |x| of 8 bf16 values, accumulated in packed form: with the sign
 // bits cleared, bf16 values compare like their bit patterns, and max.bf16x2
 // selects exactly.

@@ -8,7 +8,9 @@
 // HBM-bound.  One persistent block per SM: a producer warp keeps up to NS row
 // loads in flight through a ring of stages, and NC consumer warps quantise
 // and store, so both the bytes in flight and the quantisation warps are
-// bounded by shared memory rather than registers.
+// bounded by shared memory rather than registers.  The producer claims
+// tokens two at a time from one global counter, so SMs that move rows
+// faster take more of them (the SMs of one GB300 do not stream at one rate).
 //
 // Destinations:  normal  -- the handle's (rank, row-in-rank) list + the
 //                           rank's region offset (the layout's output);
@@ -30,12 +32,16 @@ namespace ep {
 //   [rank_offset: R+1 ints (normal) | expert_offset: E+1 ints (expert-major)]
 //   [full[NS], empty[NS] mbarriers]
 //   [NS row stages of 2H bytes][NC quantised-row buffers of H + scales (FP8)]
-// Warp 0 is the producer: lane 0 streams the block's token rows into the
-// stages with bulk loads (full[s] counts the bytes).  Warps 1..NC are
-// consumers: consumer c takes the block's tokens c, c+NC, ...; it waits for
+// Warp 0 is the producer: lane 0 streams claimed token rows into the stages
+// with bulk loads (full[s] counts the bytes), item i into stage i % NS.
+// Warps 1..NC are consumers: consumer c takes items c, c+NC, ...; it waits for
 // its stage, quantises it into its own buffer (FP8) or stores straight from
 // the stage (BF16), releases the stage (empty[s]) once nothing reads it any
-// more, and bulk-stores the row to every destination.
+// more, and bulk-stores the row to every destination.  NS is a multiple of
+// NC, so consumer c is the only one to use stages s = c (mod NC): when it
+// waits on a stage's parity for item i, it has itself consumed item i - NS
+// of that stage, so the barrier cannot still be one phase behind (a parity
+// wait would return at once on the phase before).
 __host__ __device__ inline int scatter_head_ints(int mode, int R, int E) {
   return mode == kSrcRanks ? R + 1 : mode == kSrcExpertMajor ? E + 1 : 0;
 }
@@ -44,7 +50,7 @@ __host__ __device__ inline size_t scatter_qbuf_bytes(int H) {
   return static_cast<size_t>(H) + ((4 * static_cast<size_t>(H / 128) + 15) & ~15ull);
 }
 __host__ __device__ inline size_t scatter_block_bytes(int H, int head_ints, bool fp8, int NS, int NC) {
-  return scatter_head_bytes(head_ints) + 16 * static_cast<size_t>(NS) +
+  return scatter_head_bytes(head_ints) + 16 * static_cast<size_t>(NS) + ((4 * static_cast<size_t>(NS) + 15) & ~15ull) +
          static_cast<size_t>(NS) * 2 * static_cast<size_t>(H) + (fp8 ? static_cast<size_t>(NC) * scatter_qbuf_bytes(H) : 0);
 }
 
@@ -62,7 +68,8 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_scatter(
   int* so = reinterpret_cast<int*>(smem);  // rank_offset (normal) / expert_offset (expert-major)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + scatter_head_bytes(scatter_head_ints(kMode, a.R, a.E)));
   uint64_t* empty = full + NS;
-  unsigned char* stage0 = reinterpret_cast<unsigned char*>(empty + NS);
+  int* stage_tok = reinterpret_cast<int*>(empty + NS);  // token held by each stage (-1: no more)
+  unsigned char* stage0 = reinterpret_cast<unsigned char*>(stage_tok) + ((4 * NS + 15) & ~15);
   unsigned char* qbuf0 = stage0 + static_cast<size_t>(NS) * row_bytes;
   auto stage = [&](int s) { return stage0 + static_cast<size_t>(s) * row_bytes; };
 
@@ -88,18 +95,35 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_scatter(
     mbar_init_fence();
   }
   __syncthreads();
-  // this block's tokens: blockIdx.x + i * gridDim.x
-  const int n_blk = static_cast<int>(blockIdx.x) < a.T ? (a.T - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x : 0;
 
   if (warp == 0) {
-    // producer
+    // producer: claims tokens kClaimTokens at a time (one claim ahead); when
+    // the claims run out it hands every consumer warp a "no more" stage
     if (lane == 0) {
-      for (int i = 0; i < n_blk; ++i) {
-        const int s = i % NS;
-        if (i >= NS && !mbar_wait(empty + s, static_cast<uint32_t>((i / NS - 1) & 1), a.err)) break;
-        const int t = blockIdx.x + i * gridDim.x;
-        mbar_arrive_expect_tx(full + s, row_bytes);
-        bulk_load(stage(s), a.x + static_cast<size_t>(t) * H, row_bytes, full + s);
+      unsigned* claim = a.ctl + kCtlClaim;
+      int base = static_cast<int>(atomicAdd(claim, static_cast<unsigned>(kClaimTokens)));
+      int next = base < a.T ? static_cast<int>(atomicAdd(claim, static_cast<unsigned>(kClaimTokens))) : a.T;
+      int i = 0;
+      bool ok = true;
+      while (ok && base < a.T) {
+        for (int c = 0; c < kClaimTokens && base + c < a.T; ++c, ++i) {
+          const int s = i % NS;
+          if (i >= NS && !mbar_wait(empty + s, static_cast<uint32_t>((i / NS - 1) & 1), a.err)) {
+            ok = false;
+            break;
+          }
+          stage_tok[s] = base + c;
+          mbar_arrive_expect_tx(full + s, row_bytes);
+          bulk_load(stage(s), a.x + static_cast<size_t>(base + c) * H, row_bytes, full + s);
+        }
+        base = next;
+        if (base < a.T) next = static_cast<int>(atomicAdd(claim, static_cast<unsigned>(kClaimTokens)));
+      }
+      for (int j = i; ok && j < i + NC; ++j) {
+        const int s = j % NS;
+        if (j >= NS && !mbar_wait(empty + s, static_cast<uint32_t>((j / NS - 1) & 1), a.err)) break;
+        stage_tok[s] = -1;
+        mbar_arrive(full + s);
       }
     }
     return;
@@ -110,10 +134,18 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_scatter(
   float* sd = reinterpret_cast<float*>(qd + H);
   const bool meta = !kLL && (a.recv_src_idx || a.recv_topk_idx || a.recv_topk_weights);
   bool first = true;
-  for (int i = cc; i < n_blk; i += NC) {
-    const int t = blockIdx.x + i * gridDim.x;
+  for (int i = cc;; i += NC) {
     const int s = i % NS;
-    // destinations of this token (overlaps the row load)
+    const bool landed = mbar_wait(full + s, static_cast<uint32_t>((i / NS) & 1), a.err);
+    if (!__all_sync(kFullMask, landed)) break;  // gave up (latched)
+    const int t = stage_tok[s];
+    if (t >= a.T) latch_error(a.err, kErrState);  // never written by the producer: cannot happen
+    if (t < 0 || t >= a.T) {  // no more rows
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + s);
+      break;
+    }
+    // destinations of this token
     long long row = -1;
     int r = -1, e = -1;
     float w = 0.0f;
@@ -144,8 +176,6 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_scatter(
       if (kEM && row >= 0 && a.recv_weights) w = a.topk_weights[static_cast<size_t>(t) * a.k + lane];
     }
     const unsigned dmask = __ballot_sync(kFullMask, row >= 0);
-    const bool landed = mbar_wait(full + s, static_cast<uint32_t>((i / NS) & 1), a.err);
-    if (!__all_sync(kFullMask, landed)) break;  // gave up (latched)
 
     if (kFP8) {
       if (!first) {
@@ -208,24 +238,36 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_scatter(
   }
   if (lane == 0) bulk_wait_all();  // stores done before the block's shared memory goes away
   __syncwarp();
+  // the last block to finish resets the claim counter for the next launch
+  // (every claim of every block has returned by the time it counts itself)
+  consumer_sync(NC * 32);
+  if (threadIdx.x == 32 && atomicAdd(a.ctl + kCtlDone, 1u) == gridDim.x - 1) {
+    atomicExch(a.ctl + kCtlClaim, 0u);
+    atomicExch(a.ctl + kCtlDone, 0u);
+  }
 }
 
 // Consumers and stages for a block: FP8 wants compute warps (8 consumers, the
 // rest of shared memory as stages); BF16 only moves bytes (4 consumers, more
-// stages).  Fewer consumers if the rows are long; 0 if not even two stages fit.
+// stages).  NS is a multiple of NC.  Fewer consumers if the rows are long; 0
+// if not even two stages fit.
 void scatter_config(int H, int R, int E, bool fp8, int mode, size_t smem_limit, int* NS, int* NC) {
   *NS = 0;
   *NC = 0;
-  for (int nc = fp8 ? kScatterMaxConsumers : 4; nc >= 1; --nc) {
-    const size_t fixed = scatter_block_bytes(H, scatter_head_ints(mode, R, E), fp8, 0, nc);
-    if (fixed >= smem_limit) continue;
-    const size_t per_stage = 16 + 2 * static_cast<size_t>(H);
-    int ns = static_cast<int>((smem_limit - fixed) / per_stage);
-    if (ns > 32) ns = 32;
-    if (ns >= 2) {
-      *NS = ns;
-      *NC = nc;
-      return;
+  const int max_nc = fp8 ? kScatterMaxConsumers : 4;
+  for (int pass = 0; pass < 2 && *NS == 0; ++pass) {
+    // first at least half the consumers (the quantiser's compute), then any
+    for (int nc = max_nc; nc >= (pass == 0 ? (max_nc + 1) / 2 : 1); --nc) {
+      const size_t fixed = scatter_block_bytes(H, scatter_head_ints(mode, R, E), fp8, 0, nc);
+      if (fixed >= smem_limit) continue;
+      int ns = static_cast<int>((smem_limit - fixed) / (20 + 2 * static_cast<size_t>(H)));
+      if (ns > 32) ns = 32;
+      while (ns >= 2 && scatter_block_bytes(H, scatter_head_ints(mode, R, E), fp8, ns, nc) > smem_limit) --ns;
+      ns -= ns % nc;  // consumer c owns the stages s = c (mod nc): see the kernel
+      if (ns >= 2 && ns >= nc && ns > *NS) {  // the most stages; more consumers on a tie
+        *NS = ns;
+        *NC = nc;
+      }
     }
   }
 }
