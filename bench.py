@@ -354,44 +354,79 @@ def time_ops(step: Step, K: int, stream: torch.cuda.Stream):
 
 
 def e2e_steps(step: Step, K: int, stream: torch.cuda.Stream):
-    """The same step through the public API with host buffers: inputs copied
-    host->device from pinned memory and the combine outputs copied back, every
-    step, inside the timed region."""
+    """The same step through the public API with host buffers: every input
+    copied host->device from pinned memory and every combine output copied
+    back, each step, inside the timed region.  The copies run on a second
+    stream so that they overlap the kernels, as a caller would arrange it;
+    each op waits for the copies of its own inputs.  The low-latency expert
+    outputs arrive packed (one copy) and are placed into the [E][M][H] layout
+    on the device once the host has read the step's per-expert counts."""
     pin = {}
     for name in ("x", "idx", "wts", "y", "grad_out", "grad_recv"):
         t = getattr(step, name)
         pin[name] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
         pin[name].copy_(t)
-    H = step.w.H
+    H, E, M = step.w.H, step.w.E, step.M
     y_ll_packed = step.y_ll.view(-1, H)[step.ll_rows]
     pin["y_ll"] = torch.empty(y_ll_packed.shape, dtype=y_ll_packed.dtype, pin_memory=True)
     pin["y_ll"].copy_(y_ll_packed)
+    staging = torch.empty_like(y_ll_packed)
     outs = {n: torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
             for n in ("out", "grad_x", "out_ll")}
-    counts = torch.empty(step.w.E, dtype=torch.int32, pin_memory=True)
-    h2d = sum(p.numel() * p.element_size() for p in pin.values())
+    counts = torch.empty(E, dtype=torch.int32, pin_memory=True)
+    rows_pin = torch.empty(y_ll_packed.shape[0], dtype=torch.int64, pin_memory=True)
+    rows_dev = torch.empty(y_ll_packed.shape[0], dtype=torch.int64, device=step.dev)
+    h2d = sum(p.numel() * p.element_size() for p in pin.values()) + rows_pin.numel() * 8
     d2h = sum(o.numel() * o.element_size() for o in outs.values()) + counts.numel() * 4
     ops = dict(step.ops())
+    cs = torch.cuda.Stream(step.dev)
+    ev = {n: torch.cuda.Event() for n in ("in", "y", "go", "gr", "yl", "out", "gx", "rows")}
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(K):
-        for name in ("x", "idx", "wts", "y", "grad_out", "grad_recv"):
-            getattr(step, name).copy_(pin[name], non_blocking=True)
-        for name in ("layout_dispatch_fp8", "combine", "dispatch_bf16_bwd", "combine_bwd", "ll_dispatch_fp8"):
-            ops[name]()
+        cs.wait_stream(stream)  # the previous step no longer reads the inputs
+        with torch.cuda.stream(cs):
+            for name in ("x", "idx", "wts"):
+                getattr(step, name).copy_(pin[name], non_blocking=True)
+            ev["in"].record(cs)
+            step.y.copy_(pin["y"], non_blocking=True)
+            ev["y"].record(cs)
+            step.grad_out.copy_(pin["grad_out"], non_blocking=True)
+            ev["go"].record(cs)
+            step.grad_recv.copy_(pin["grad_recv"], non_blocking=True)
+            ev["gr"].record(cs)
+            staging.copy_(pin["y_ll"], non_blocking=True)
+            ev["yl"].record(cs)
+        stream.wait_event(ev["in"])
+        ops["layout_dispatch_fp8"]()
+        stream.wait_event(ev["y"])
+        ops["combine"]()
+        ev["out"].record(stream)
+        stream.wait_event(ev["go"])
+        ops["dispatch_bf16_bwd"]()
+        stream.wait_event(ev["gr"])
+        ops["combine_bwd"]()
+        ev["gx"].record(stream)
+        with torch.cuda.stream(cs):
+            cs.wait_event(ev["out"])
+            outs["out"].copy_(step.out, non_blocking=True)
+            cs.wait_event(ev["gx"])
+            outs["grad_x"].copy_(step.grad_x, non_blocking=True)
+        ops["ll_dispatch_fp8"]()
         counts.copy_(step.ll_cnt, non_blocking=True)
         stream.synchronize()
-        row = 0
-        yl = step.y_ll
-        for e, c in enumerate(counts.tolist()):
-            if c:
-                yl[e, :c].copy_(pin["y_ll"][row:row + c], non_blocking=True)
-                row += c
+        c = counts.numpy().astype(np.int64)
+        if int(c.sum()) != rows_pin.numel():
+            raise RuntimeError("low-latency counts changed between steps of one batch")
+        starts = np.repeat(np.arange(E, dtype=np.int64) * M - np.concatenate([[0], np.cumsum(c)[:-1]]), c)
+        rows_pin.numpy()[:] = starts + np.arange(c.sum(), dtype=np.int64)
+        rows_dev.copy_(rows_pin, non_blocking=True)
+        stream.wait_event(ev["yl"])
+        step.y_ll.view(-1, H).index_copy_(0, rows_dev, staging)
         ops["ll_combine"]()
-        outs["out"].copy_(step.out, non_blocking=True)
-        outs["grad_x"].copy_(step.grad_x, non_blocking=True)
         outs["out_ll"].copy_(step.out_ll, non_blocking=True)
         stream.synchronize()
+        cs.synchronize()
     dt = time.perf_counter() - t0
     return dt, h2d, d2h
 

@@ -51,7 +51,7 @@ struct ep_handle {
   int* em_slot;
   int* em_count;
   int* em_offset;
-  int* fused_agg;               // [num_sms][R+E] per-block counts of the fused kernel
+  uint16_t* fused_agg;          // [num_sms][R+E padded to 8] per-block counts of the fused kernel
   unsigned* fused_barrier;      // [4 + num_sms] its control words (barrier, row claims, published flags)
   size_t smem_optin;
   int* err;
@@ -246,7 +246,7 @@ ep_status_t ep_handle_create(int R, int E, int k, int H, int max_tpr, ep_handle_
   const size_t o_emslot = take(sizeof(int) * static_cast<size_t>(h->Tmax) * k);
   const size_t o_emcnt = take(sizeof(int) * E);
   const size_t o_emoff = take(sizeof(int) * (E + 1));
-  const size_t o_fagg = take(sizeof(int) * static_cast<size_t>(h->num_sms) * (R + E));
+  const size_t o_fagg = take(sizeof(uint16_t) * static_cast<size_t>(h->num_sms) * ((R + E + 7) & ~7));
   const size_t o_fbar = take(sizeof(unsigned) * (4 + static_cast<size_t>(h->num_sms)));
   const size_t o_err = take(sizeof(int));
   if ((st = cuda_status(cudaMalloc(&h->arena, off), "cudaMalloc")) != EP_OK) {
@@ -269,7 +269,7 @@ ep_status_t ep_handle_create(int R, int E, int k, int H, int max_tpr, ep_handle_
   h->em_slot = reinterpret_cast<int*>(base + o_emslot);
   h->em_count = reinterpret_cast<int*>(base + o_emcnt);
   h->em_offset = reinterpret_cast<int*>(base + o_emoff);
-  h->fused_agg = reinterpret_cast<int*>(base + o_fagg);
+  h->fused_agg = reinterpret_cast<uint16_t*>(base + o_fagg);
   h->fused_barrier = reinterpret_cast<unsigned*>(base + o_fbar);
   h->err = reinterpret_cast<int*>(base + o_err);
   // zero everything once (latch, look-back words); tickets start at epoch 1,

@@ -86,65 +86,87 @@ __device__ inline void grid_sync(unsigned* words, unsigned g, unsigned nblocks, 
 
 __host__ __device__ inline int fused_tokens_per_block(int T, int nb) { return (T + nb - 1) / nb; }
 
-// Column `col` of the per-block counts summed over blocks q < b (exclusive)
-// and over all blocks.  Loads are issued 32 at a time before any is added, so
-// a column costs one L2 round trip per 32 blocks.
-__device__ __forceinline__ void column_sums(const int* agg, int NK, int col, int nb, int b, int* ex, int* all) {
-  int e = 0, a = 0;
+// The per-block counts (FusedArgs::agg) are uint16 -- a block owns at most
+// kFusedMaxItems (token, k) entries -- in rows of agg_ld(NK) entries (a
+// multiple of 8, so a row is a whole number of 16-byte words).
+__host__ __device__ inline int agg_ld(int NK) { return (NK + 7) & ~7; }
+
+// Column `col` of the per-block counts summed over every block (off the
+// critical path: loads issued 32 at a time).
+__device__ __forceinline__ int column_total(const uint16_t* agg, int ld, int col, int nb) {
+  int all = 0;
   for (int q0 = 0; q0 < nb; q0 += 32) {
     int v[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = q0 + j < nb ? __ldcg(agg + static_cast<size_t>(q0 + j) * NK + col) : 0;
+    for (int j = 0; j < 32; ++j) v[j] = q0 + j < nb ? __ldcg(agg + static_cast<size_t>(q0 + j) * ld + col) : 0;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      a += v[j];
-      if (q0 + j < b) e += v[j];
-    }
+    for (int j = 0; j < 32; ++j) all += v[j];
   }
-  *ex = e;
-  *all = a;
+  return all;
 }
 
-// Columns [0, ncols) of the per-block counts (row q = block q's counts, NK
-// ints per row): excl[c] = the sum over blocks q < b and, if `all` is given,
-// all[c] = the sum over every block.  tpc threads share a column (a power of
-// two up to 32, so they sit in one warp); each thread issues its loads 32 at a
-// time before adding any, then one shuffle reduction per column: a column
-// costs about one L2 round trip per 32 * tpc blocks.
-__device__ inline void column_sums_par(const int* agg, int NK, int ncols, int nb, int b, int* excl, int* all, int nct,
-                                       int ct) {
+// Columns [0, ncols) of the per-block counts: excl[c] = the sum over blocks
+// q < b and, if `all` is given, all[c] = the sum over every block.  A thread
+// loads 8 columns at a time (one 16-byte word per block row); tpc threads
+// share an 8-column group (a power of two up to 32, so they sit in one warp)
+// and issue their loads 16 words at a time before adding any, then one
+// shuffle reduction: a group costs about one L2 round trip per 16 * tpc
+// blocks.
+__device__ inline void column_sums_par(const uint16_t* agg, int ld, int ncols, int nb, int b, int* excl, int* all,
+                                       int nct, int ct) {
+  const int oct = (ncols + 7) >> 3;
   int tpc = 32;
-  while (tpc > 1 && tpc * ncols > nct) tpc >>= 1;
+  while (tpc > 1 && tpc * oct > nct) tpc >>= 1;
   const int groups = nct / tpc;
   const int sub = ct & (tpc - 1);
   const int qend = all ? nb : b;
-  for (int c0 = 0; c0 < ncols; c0 += groups) {  // the same trip count in every thread
+  for (int c0 = 0; c0 < oct; c0 += groups) {  // the same trip count in every thread
     const int c = c0 + ct / tpc;
-    const bool valid = c < ncols;
-    int e = 0, s = 0;
-    if (valid) {
-      for (int q0 = sub; q0 < qend; q0 += 32 * tpc) {
-        int v[32];
+    const bool valid = c < oct;
+    int e[8], s[8];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+    for (int i = 0; i < 8; ++i) e[i] = s[i] = 0;
+    if (valid) {
+      for (int q0 = sub; q0 < qend; q0 += 16 * tpc) {
+        uint4 v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
           const int q = q0 + j * tpc;
-          v[j] = q < qend ? __ldcg(agg + static_cast<size_t>(q) * NK + c) : 0;
+          v[j] = q < qend ? __ldcg(reinterpret_cast<const uint4*>(agg + static_cast<size_t>(q) * ld) + c)
+                          : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          s += v[j];
-          if (q0 + j * tpc < b) e += v[j];
+        for (int j = 0; j < 16; ++j) {
+          const bool before = q0 + j * tpc < b;
+          const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int lo = static_cast<int>(w[i] & 0xffffu), hi = static_cast<int>(w[i] >> 16);
+            s[2 * i] += lo;
+            s[2 * i + 1] += hi;
+            if (before) {
+              e[2 * i] += lo;
+              e[2 * i + 1] += hi;
+            }
+          }
         }
       }
     }
-    for (int d = tpc >> 1; d >= 1; d >>= 1) {
-      e += __shfl_xor_sync(kFullMask, e, d);
-      s += __shfl_xor_sync(kFullMask, s, d);
-    }
-    if (valid && sub == 0) {
-      excl[c] = e;
-      if (all) all[c] = s;
-    }
+    for (int d = tpc >> 1; d >= 1; d >>= 1)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        e[i] += __shfl_xor_sync(kFullMask, e[i], d);
+        s[i] += __shfl_xor_sync(kFullMask, s[i], d);
+      }
+    if (valid && sub == 0)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int col = 8 * c + i;
+        if (col < ncols) {
+          excl[col] = e[i];
+          if (all) all[col] = s[i];
+        }
+      }
   }
 }
 
@@ -355,9 +377,9 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
         cnt[w * R + col] = run;
         run += v;
       }
-      a.agg[static_cast<size_t>(b) * (R + E) + col] = run;
+      a.agg[static_cast<size_t>(b) * agg_ld(R + E) + col] = static_cast<uint16_t>(run);
     }
-    for (int e = ct; e < E; e += nct) a.agg[static_cast<size_t>(b) * (R + E) + R + e] = hist[e];
+    for (int e = ct; e < E; e += nct) a.agg[static_cast<size_t>(b) * agg_ld(R + E) + R + e] = static_cast<uint16_t>(hist[e]);
   } else {
     const int NI = tpb << a.kp_log2;
     const int ipw = (((NI + NC - 1) / NC) + 31) & ~31;
@@ -397,15 +419,15 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
         cnt[w * E + col] = run;
         run += v;
       }
-      a.agg[static_cast<size_t>(b) * E + col] = run;
+      a.agg[static_cast<size_t>(b) * agg_ld(E) + col] = static_cast<uint16_t>(run);
     }
   }
 
   // ---------------------------------------------------------------- phase 2: prefixes over blocks
   grid_sync(a.barrier, gen, static_cast<unsigned>(nb), a.err, nct);
-  const int NK = kLL ? E : R + E;
+  const int ld = agg_ld(kLL ? E : R + E);
   if (!kLL) {
-    column_sums_par(a.agg, NK, R, nb, b, excl, tot, nct, ct);
+    column_sums_par(a.agg, ld, R, nb, b, excl, tot, nct, ct);
     consumer_sync(nct);
     if (cw == 0) {  // exclusive scan of the rank totals -> region offsets
       const int v = lane < R ? tot[lane] : 0;
@@ -454,7 +476,7 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
       for (; pos < kmax; ++pos) a.dst[static_cast<size_t>(t) * kmax + pos] = make_int2(-1, -1);
     }
   } else {
-    column_sums_par(a.agg, NK, E, nb, b, excl, kEM ? etot : nullptr, nct, ct);
+    column_sums_par(a.agg, ld, E, nb, b, excl, kEM ? etot : nullptr, nct, ct);
     consumer_sync(nct);
     if (kEM) {
       // group offsets: each consumer thread takes a contiguous run of experts
@@ -639,8 +661,7 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
   // per-expert totals (outputs only, nothing above waits for them): block b
   // forms the totals of experts e = b, b + nb, ...
   for (int e = b + ct * nb; !kEM && e < E; e += nct * nb) {
-    int ex, all;
-    column_sums(a.agg, NK, (kLL ? 0 : R) + e, nb, 0, &ex, &all);
+    const int all = column_total(a.agg, ld, (kLL ? 0 : R) + e, nb);
     if (kLL) {
       if (a.recv_count) a.recv_count[e] = min(all, a.M);
     } else {

@@ -151,7 +151,7 @@ struct FusedArgs {
   const uint16_t* x;
   const float* topk_weights;
   int T, R, E, El, k, kp_log2, kmax, H, M;
-  int* agg;           // [blocks][R+E] (normal) or [blocks][E] (low latency)
+  uint16_t* agg;      // per-block counts [blocks][R+E] (normal) or [blocks][E], rows padded to 8
   unsigned* barrier;  // [4 + blocks] control words: grid barrier, row claims, published flags
   int* err;
   // normal mode: the handle's layout state and the dispatch outputs
