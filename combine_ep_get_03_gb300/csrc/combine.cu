@@ -17,7 +17,9 @@
 //  expert-major: out[t] = bf16( sum of fp32(y[row_j]) ) over t's unmasked
 //                entries in ascending expert id, from +0.0 with RN adds.
 //
-// HBM-bound gather-reduce.  Work is split into (token, 1024-channel part)
+// HBM-bound gather-reduce.  Two blocks per SM (at most 128 registers a
+// thread): the e4m3 variant, which needs the most registers, is latency-bound
+// with one.  Work is split into (token, 1024-channel part)
 // items dealt round-robin to the warps of a persistent grid, so the last
 // round leaves few warps idle.  A warp takes a part one slab at a time (512
 // bf16 or 1024 e4m3 channels) and requests every source row of the slab
@@ -51,7 +53,7 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes) {
 }
 
 template <int kSrc, bool kFP8>
-__global__ void __launch_bounds__(kCombineThreads) k_combine(CombineArgs a) {
+__global__ void __launch_bounds__(kCombineThreads, 2) k_combine(CombineArgs a) {
   extern __shared__ int base_smem[];  // rank_offset [R+1] or expert_offset [E+1]
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
