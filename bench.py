@@ -42,15 +42,18 @@ OPS = ["layout_dispatch_fp8", "combine", "dispatch_bf16_bwd", "combine_bwd", "ll
 KERNEL_OF = {"layout_dispatch_fp8": "k_route_scatter<fp8>", "combine": "k_combine<normal>",
              "dispatch_bf16_bwd": "k_scatter<bf16>", "combine_bwd": "k_combine<normal>",
              "ll_dispatch_fp8": "k_route_scatter<fp8,ll>", "ll_combine": "k_combine<ll>"}
-KERNEL_SOURCES = {"k_combine<normal>": ["combine.cu", "device_common.cuh"],
-                  "k_combine<ll>": ["combine.cu", "device_common.cuh"],
-                  "k_route_scatter<fp8>": ["dispatch_fused.cu", "scatter_common.cuh", "device_common.cuh"],
-                  "k_route_scatter<fp8,ll>": ["dispatch_fused.cu", "scatter_common.cuh", "device_common.cuh"],
-                  "k_scatter<bf16>": ["scatter_tma.cu", "scatter_common.cuh", "device_common.cuh"]}
+KERNEL_SOURCES = {"k_combine<normal>": ["combine.cu", "device_common.cuh", "ep_internal.h"],
+                  "k_combine<ll>": ["combine.cu", "device_common.cuh", "ep_internal.h"],
+                  "k_route_scatter<fp8>": ["dispatch_fused.cu", "scatter_common.cuh", "device_common.cuh",
+                                           "ep_internal.h"],
+                  "k_route_scatter<fp8,ll>": ["dispatch_fused.cu", "scatter_common.cuh", "device_common.cuh",
+                                              "ep_internal.h"],
+                  "k_scatter<bf16>": ["scatter_tma.cu", "scatter_common.cuh", "device_common.cuh", "ep_internal.h"]}
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
 # ncu capture of the V3-shaped workload, keyed by the kernel's source digest:
 # a kernel whose sources changed since its capture reports traffic = null.
-MEASURED_TRAFFIC = {"k_combine<normal>": ("09f59f9100e60039", 712760064)}
+MEASURED_TRAFFIC = {"k_combine<normal>": ("5f0788197b1d350a", 713007616),
+                    "k_route_scatter<fp8>": ("09f840dd24291bf0", 382813952)}
 
 
 def kernel_digest(kernel: str) -> str:
