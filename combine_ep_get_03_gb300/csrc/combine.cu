@@ -52,6 +52,15 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes) {
   return make_float2(lo, hi);
 }
 
+// (a0, a1) += (p0, p1) * s: two RN multiplies, then two RN adds.  Scalar
+// intrinsics on purpose: a packed mul.rn.f32x2 followed by add.rn.f32x2 was
+// measured to come out as a fused multiply-add (one rounding), which is not
+// this sum.
+__device__ __forceinline__ void add_scaled2(float& a0, float& a1, float p0, float p1, float s) {
+  a0 = __fadd_rn(a0, __fmul_rn(p0, s));
+  a1 = __fadd_rn(a1, __fmul_rn(p1, s));
+}
+
 template <int kSrc, bool kFP8>
 __global__ void __launch_bounds__(kCombineThreads, 2) k_combine(CombineArgs a) {
   extern __shared__ int base_smem[];  // rank_offset [R+1] or expert_offset [E+1]
@@ -135,11 +144,14 @@ __global__ void __launch_bounds__(kCombineThreads, 2) k_combine(CombineArgs a) {
       for (int c = 0; c < kChunks; ++c)
 #pragma unroll
         for (int i = 0; i < kLaneCh; ++i) acc[c][i] = 0.0f;
-      for (int sb = 0; sb < n; sb += kMaxSrc) {
-        uint4 v[kMaxSrc][kChunks];
-        float sc[kMaxSrc][kChunks];
+      // sources loaded together: e4m3 rows take half the batch (fewer
+      // registers, so two blocks fit an SM; 16 channels per chunk already)
+      constexpr int kBatch = kFP8 ? kMaxSrc / 2 : kMaxSrc;
+      for (int sb = 0; sb < n; sb += kBatch) {
+        uint4 v[kBatch][kChunks];
+        float sc[kBatch][kChunks];
 #pragma unroll
-        for (int s = 0; s < kMaxSrc; ++s) {
+        for (int s = 0; s < kBatch; ++s) {
           const long long r_ = __shfl_sync(kFullMask, srow, (sb + s) & 31);
           if (sb + s < n) {
 #pragma unroll
@@ -157,7 +169,7 @@ __global__ void __launch_bounds__(kCombineThreads, 2) k_combine(CombineArgs a) {
           }
         }
 #pragma unroll
-        for (int s = 0; s < kMaxSrc; ++s) {
+        for (int s = 0; s < kBatch; ++s) {
           const float ws = __shfl_sync(kFullMask, sw, (sb + s) & 31);
           if (sb + s < n) {
 #pragma unroll
@@ -168,10 +180,8 @@ __global__ void __launch_bounds__(kCombineThreads, 2) k_combine(CombineArgs a) {
                 if (kFP8) {
                   const float2 f01 = e4m3x2_to_float2(q[i] & 0xffffu);
                   const float2 f23 = e4m3x2_to_float2(q[i] >> 16);
-                  acc[c][4 * i] = __fadd_rn(acc[c][4 * i], __fmul_rn(f01.x, sc[s][c]));
-                  acc[c][4 * i + 1] = __fadd_rn(acc[c][4 * i + 1], __fmul_rn(f01.y, sc[s][c]));
-                  acc[c][4 * i + 2] = __fadd_rn(acc[c][4 * i + 2], __fmul_rn(f23.x, sc[s][c]));
-                  acc[c][4 * i + 3] = __fadd_rn(acc[c][4 * i + 3], __fmul_rn(f23.y, sc[s][c]));
+                  add_scaled2(acc[c][4 * i], acc[c][4 * i + 1], f01.x, f01.y, sc[s][c]);
+                  add_scaled2(acc[c][4 * i + 2], acc[c][4 * i + 3], f23.x, f23.y, sc[s][c]);
                 } else if (kSrc == kSrcLowLatency) {
                   acc[c][2 * i] = __fmaf_rn(ws, bf16_lo(q[i]), acc[c][2 * i]);
                   acc[c][2 * i + 1] = __fmaf_rn(ws, bf16_hi(q[i]), acc[c][2 * i + 1]);

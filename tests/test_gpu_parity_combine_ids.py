@@ -184,3 +184,28 @@ def test_int32_ids_from_environment(monkeypatch):
     h = ep.Handle(4, 16, 2, 128, 8)
     assert h.topk_idx_bits == 64
     h.close()
+
+
+def test_combine_ex_v3_workload():
+    """Full V3 shape: the e4m3 rows of the fused dispatch combined back, with
+    the weights' reduction, against the oracle."""
+    w_ = wl.WORKLOADS["v3_ep8"]
+    x, idx, wts = wl.make_inputs(w_)
+    R, E, k, H, T = w_.R, w_.E, w_.k, w_.H, w_.T
+    L = oracle.layout(R, E, k, idx)
+    P = int(L["rank_offset"][-1])
+    h = ep.Handle(R, E, k, H, w_.tokens_per_rank)
+    recv = torch.empty((P, H), dtype=torch.uint8, device=DEV)
+    sc = torch.empty((P, H // 128), dtype=torch.float32, device=DEV)
+    rw = torch.empty((P, k), dtype=torch.float32, device=DEV)
+    h.layout_and_dispatch(dev(idx), dev(x), dev(wts), ep.EP_FP8_E4M3, recv, sc, recv_topk_weights=rw)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    cw = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    h.combine_ex(recv, out, y_scales=sc, recv_topk_weights=rw, combined_topk_weights=cw)
+    ref_out, ref_cw = oracle.combine_ex(R, E, k, idx, recv.cpu().numpy(), y_scales=sc.cpu().numpy(),
+                                        recv_topk_weights=rw.cpu().numpy())
+    assert assert_bf16_close(host_bits(out), ref_out, "e4m3 combine, V3 shape") == 1.0
+    assert np.array_equal(cw.cpu().numpy().view(np.uint32), ref_cw.view(np.uint32))
+    assert np.array_equal(cw.cpu().numpy(), np.where(idx >= 0, wts, np.float32(0)))
+    assert h.get_device_status() == ep.EP_OK
+    h.close()
