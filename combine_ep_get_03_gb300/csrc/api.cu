@@ -132,6 +132,7 @@ ep::FusedArgs fused_args(ep_handle* h, const void* topk_idx, const uint16_t* x, 
   ep::FusedArgs f{};
   f.topk_idx = topk_idx;
   f.ids32 = h->ids32;
+  f.redundant = static_cast<long long>(T) * h->k <= ep::kFusedRedundantEntries ? 1 : 0;  // per-entry modes only
   f.x = x;
   f.topk_weights = w;
   f.T = T;

@@ -164,6 +164,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
   return false;
 }
 
+// A 4-byte store that the L2 keeps ahead of streaming data (evict_last).
+// For metadata scattered one word per row: the 32-byte sector of such a word
+// is completed by other rows written much later, and a sector evicted half
+// written costs the DRAM a read-modify-write.
+__device__ __forceinline__ void st_keep(float* p, float v) {
+  unsigned long long pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" : : "l"(p), "f"(v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_keep(int* p, int v) {
+  unsigned long long pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  asm volatile("st.global.L2::cache_hint.s32 [%0], %1, %2;" : : "l"(p), "r"(v), "l"(pol) : "memory");
+}
+
 // Expert id i of a top-k table held as int64 (ids32 == 0) or int32.
 __device__ __forceinline__ long long load_topk_id(const void* topk_idx, long long i, int ids32) {
   return ids32 ? static_cast<long long>(static_cast<const int*>(topk_idx)[i])

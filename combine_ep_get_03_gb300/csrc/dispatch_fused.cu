@@ -177,7 +177,7 @@ __host__ __device__ inline size_t fused_route_bytes(int mode, int R, int E, int 
            + 4 * static_cast<size_t>(tpb) * kmax               // local rows
            + 4 * (static_cast<size_t>(nc) * R + E + 3 * (R + 1) + 4);
   const size_t ni = static_cast<size_t>(tpb) * kp;
-  const size_t em = mode == kSrcExpertMajor ? 2 * static_cast<size_t>(E) + 1 + 32 : 0;  // totals, offsets, scan
+  const size_t em = 2 * static_cast<size_t>(E) + 1 + 32;  // totals, group offsets, scan scratch
   return 8 * ni + 4 * (static_cast<size_t>(nc) * E + E + 4 + em);
 }
 
@@ -253,11 +253,9 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
     item_slot = item_e + tpb * kp;
     cnt = item_slot + tpb * kp;        // [NC][E], then per-warp prefixes
     excl = cnt + NC * E;               // [E]
-    if (kEM) {
-      etot = excl + E + 4;             // [E] totals
-      eoff = etot + E;                 // [E+1] group offsets
-      wsum = eoff + E + 1;             // [32] scan scratch
-    }
+    etot = excl + E + 4;               // [E] totals
+    eoff = etot + E;                   // [E+1] group offsets (expert-major)
+    wsum = eoff + E + 1;               // [32] scan scratch
   }
   unsigned char* sbase = smem + ((fused_route_bytes(kMode, R, E, kmax, kp, tpb, NC) + 127) & ~static_cast<size_t>(127));
   uint64_t* full = reinterpret_cast<uint64_t*>(sbase);
@@ -419,12 +417,37 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
         cnt[w * E + col] = run;
         run += v;
       }
-      a.agg[static_cast<size_t>(b) * agg_ld(E) + col] = static_cast<uint16_t>(run);
+      if (!a.redundant) a.agg[static_cast<size_t>(b) * agg_ld(E) + col] = static_cast<uint16_t>(run);
+    }
+    if (a.redundant) {
+      // small batches: every block counts every entry itself (entries of
+      // earlier tokens into excl, all of them into etot) instead of meeting
+      // the other blocks at the grid barrier
+      for (int e = ct; e < E; e += nct) excl[e] = etot[e] = 0;
+      consumer_sync(nct);
+      const long long n_all = static_cast<long long>(a.T) * k, n_before = static_cast<long long>(t_begin) * k;
+      for (long long i0 = ct; i0 < n_all; i0 += 16 * static_cast<long long>(nct)) {
+        long long v[16];  // 16 independent loads in flight, then the counting
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const long long i = i0 + static_cast<long long>(j) * nct;
+          v[j] = i < n_all ? load_topk_id(a.topk_idx, i, a.ids32) : -1;
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          if (v[j] >= 0 && v[j] < E) {
+            atomicAdd(etot + v[j], 1);
+            if (i0 + static_cast<long long>(j) * nct < n_before) atomicAdd(excl + v[j], 1);
+          }
+        }
+      }
     }
   }
 
   // ---------------------------------------------------------------- phase 2: prefixes over blocks
-  grid_sync(a.barrier, gen, static_cast<unsigned>(nb), a.err, nct);
+  const bool barrier = !(kLL && a.redundant);
+  if (barrier) grid_sync(a.barrier, gen, static_cast<unsigned>(nb), a.err, nct);
+  else consumer_sync(nct);
   const int ld = agg_ld(kLL ? E : R + E);
   if (!kLL) {
     column_sums_par(a.agg, ld, R, nb, b, excl, tot, nct, ct);
@@ -476,8 +499,10 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
       for (; pos < kmax; ++pos) a.dst[static_cast<size_t>(t) * kmax + pos] = make_int2(-1, -1);
     }
   } else {
-    column_sums_par(a.agg, ld, E, nb, b, excl, kEM ? etot : nullptr, nct, ct);
-    consumer_sync(nct);
+    if (!a.redundant) {
+      column_sums_par(a.agg, ld, E, nb, b, excl, kEM ? etot : nullptr, nct, ct);
+      consumer_sync(nct);
+    }
     if (kEM) {
       // group offsets: each consumer thread takes a contiguous run of experts
       const int per = (E + nct - 1) / nct;
@@ -600,7 +625,7 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
         const long long rr = __shfl_sync(kFullMask, row, sl);
         if (lane == 0) bulk_store(static_cast<uint8_t*>(a.recv_x) + rr * H, qd, static_cast<uint32_t>(H));
         if (kEM)
-          for (int g = lane; g < G; g += 32) a.recv_scales[g * a.scales_ld + rr] = sd[g];
+          for (int g = lane; g < G; g += 32) st_keep(a.recv_scales + g * a.scales_ld + rr, sd[g]);
         else
           for (int g = lane; g < G; g += 32) a.recv_scales[rr * G + g] = sd[g];
       }
@@ -628,7 +653,7 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
         m &= m - 1;
         const long long rr = __shfl_sync(kFullMask, row, sl);
         const int rk = __shfl_sync(kFullMask, r, sl);
-        if (lane == 0 && a.recv_src_idx) a.recv_src_idx[rr] = t;
+        if (lane == 0 && a.recv_src_idx) st_keep(a.recv_src_idx + rr, t);
         if (lane < k) {
           const bool here = e >= 0 && e / a.El == rk;
           if (a.recv_topk_idx) a.recv_topk_idx[rr * k + lane] = here ? e - rk * a.El : -1;
@@ -636,10 +661,10 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
         }
       }
     } else if (kEM && row >= 0) {
-      if (a.recv_src_idx) a.recv_src_idx[row] = t;
-      if (a.recv_weights) a.recv_weights[row] = w;
+      if (a.recv_src_idx) st_keep(a.recv_src_idx + row, t);
+      if (a.recv_weights) st_keep(a.recv_weights + row, w);
     } else if (kLL && a.recv_src_info && row >= 0) {
-      a.recv_src_info[row] = t;
+      st_keep(a.recv_src_info + row, t);
     }
   }
   if (kEM) {
@@ -661,7 +686,7 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
   // per-expert totals (outputs only, nothing above waits for them): block b
   // forms the totals of experts e = b, b + nb, ...
   for (int e = b + ct * nb; !kEM && e < E; e += nct * nb) {
-    const int all = column_total(a.agg, ld, (kLL ? 0 : R) + e, nb);
+    const int all = kLL && a.redundant ? etot[e] : column_total(a.agg, ld, (kLL ? 0 : R) + e, nb);
     if (kLL) {
       if (a.recv_count) a.recv_count[e] = min(all, a.M);
     } else {
@@ -672,10 +697,13 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
   __syncwarp();
   // the last block to finish resets the claim counter for the next launch
   // (every claim of every block has returned by the time it counts itself)
+  // (and, when there was no grid barrier, advances the generation that the
+  // "published" words of the next launch are compared with)
   consumer_sync(nct);
   if (threadIdx.x == 32 && atomicAdd(a.barrier + kCtlDone, 1u) == static_cast<unsigned>(nb) - 1) {
     atomicExch(a.barrier + kCtlClaim, 0u);
     atomicExch(a.barrier + kCtlDone, 0u);
+    if (!barrier) atomicAdd(a.barrier + 1, 1u);
   }
 }
 

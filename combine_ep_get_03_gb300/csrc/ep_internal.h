@@ -145,9 +145,14 @@ void launch_scatter(const ScatterArgs& a, bool fp8, int mode, int blocks, int NS
 
 // Fused routing + dispatch (cooperative launch, one block per SM).
 constexpr int kFusedMaxItems = 4096;  // (token, k) entries a block may own
+// Per-entry fused routing counts every entry in every block (no grid
+// barrier) when the batch has at most this many (token, k) entries.
+constexpr long long kFusedRedundantEntries = 16384;
+
 struct FusedArgs {
   const void* topk_idx;        // [T][k] int64, or int32 if ids32
   int ids32;
+  int redundant;               // per-entry modes: count redundantly, no grid barrier
   const uint16_t* x;
   const float* topk_weights;
   int T, R, E, El, k, kp_log2, kmax, H, M;

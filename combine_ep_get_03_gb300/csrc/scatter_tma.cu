@@ -193,7 +193,7 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_scatter(
         const long long rr = __shfl_sync(kFullMask, row, sl);
         if (lane == 0) bulk_store(static_cast<uint8_t*>(a.recv_x) + rr * H, qd, static_cast<uint32_t>(H));
         if (kEM)
-          for (int g = lane; g < G; g += 32) a.recv_scales[g * a.scales_ld + rr] = sd[g];
+          for (int g = lane; g < G; g += 32) st_keep(a.recv_scales + g * a.scales_ld + rr, sd[g]);
         else
           for (int g = lane; g < G; g += 32) a.recv_scales[rr * G + g] = sd[g];
       }
@@ -222,7 +222,7 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_scatter(
         m &= m - 1;
         const long long rr = __shfl_sync(kFullMask, row, sl);
         const int rk = __shfl_sync(kFullMask, r, sl);
-        if (lane == 0 && a.recv_src_idx) a.recv_src_idx[rr] = t;
+        if (lane == 0 && a.recv_src_idx) st_keep(a.recv_src_idx + rr, t);
         if (lane < a.k) {
           const bool here = e >= 0 && e / a.El == rk;
           if (a.recv_topk_idx) a.recv_topk_idx[rr * a.k + lane] = here ? e - rk * a.El : -1;
@@ -230,10 +230,10 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_scatter(
         }
       }
     } else if (kEM && row >= 0) {
-      if (a.recv_src_idx) a.recv_src_idx[row] = t;
-      if (a.recv_weights) a.recv_weights[row] = w;
+      if (a.recv_src_idx) st_keep(a.recv_src_idx + row, t);
+      if (a.recv_weights) st_keep(a.recv_weights + row, w);
     } else if (kLL && a.recv_src_info && row >= 0) {
-      a.recv_src_info[row] = t;
+      st_keep(a.recv_src_info + row, t);
     }
   }
   if (lane == 0) bulk_wait_all();  // stores done before the block's shared memory goes away
