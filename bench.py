@@ -52,8 +52,8 @@ KERNEL_SOURCES = {"k_combine<normal>": ["combine.cu", "device_common.cuh", "ep_i
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
 # ncu capture of the V3-shaped workload, keyed by the kernel's source digest:
 # a kernel whose sources changed since its capture reports traffic = null.
-MEASURED_TRAFFIC = {"k_combine<normal>": ("5f0788197b1d350a", 713007616),
-                    "k_route_scatter<fp8>": ("09f840dd24291bf0", 382813952)}
+MEASURED_TRAFFIC = {"k_combine<normal>": ("6ce805801263a60e", 712687616),
+                    "k_route_scatter<fp8>": ("1094c7c56ae9464e", 382835456)}
 
 
 def kernel_digest(kernel: str) -> str:
@@ -336,6 +336,37 @@ def time_steps(step: Step, K: int, stream: torch.cuda.Stream) -> float:
     for _ in range(K):
         for fn in ops:
             fn()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end)
+
+
+def time_steps_graph(step: Step, K: int, stream: torch.cuda.Stream):
+    """The same K steps launched from one CUDA graph that holds a whole step
+    (its six ABI calls, no host synchronisation inside), replayed K times
+    between two events: the launch gaps between the step's kernels shrink to
+    what the graph leaves.  Returns milliseconds, or None if capture fails."""
+    ops = [fn for _, fn in step.ops()]
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(step.dev)
+    side.wait_stream(stream)
+    try:
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                for fn in ops:
+                    fn()
+    except Exception:
+        torch.cuda.synchronize(step.dev)
+        return None
+    stream.wait_stream(side)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize(step.dev)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(K):
+        g.replay()
     end.record(stream)
     end.synchronize()
     return start.elapsed_time(end)
@@ -638,7 +669,12 @@ def main():
     barrier()
     with ClockSampler(dev) as clk:
         total_ms = time_steps(step, args.steps, stream)
+        barrier()
+        graph_ms = time_steps_graph(step, args.steps, stream)
     barrier()
+    stream_ms, timed = total_ms, "stream"
+    if graph_ms is not None and graph_ms < total_ms:
+        total_ms, timed = graph_ms, "cuda_graph"
     per_op = time_ops(step, min(args.steps, 300), stream)
     status = step.h.get_device_status()
     if status != ep.EP_OK:
@@ -690,6 +726,9 @@ def main():
                    "num_sms": args.num_sms or torch.cuda.get_device_properties(dev).multi_processor_count,
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": round(w.T * world / (total_ms / args.steps / 1e3), 1),
+        "launch": {"timed": timed,
+                   "ms_per_step_stream": round(stream_ms / args.steps, 4),
+                   "ms_per_step_graph": None if graph_ms is None else round(graph_ms / args.steps, 4)},
         "ops": ops,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
