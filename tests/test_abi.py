@@ -74,3 +74,35 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(ep, "_lib", None)
     with pytest.raises(RuntimeError, match="no fallback"):
         ep.lib()
+
+
+def test_header_is_plain_c_and_links(tmp_path):
+    """include/ep.h compiles as C99 (no C++ in the boundary) and a C program
+    links against the library and calls its host-only entry points."""
+    import subprocess
+    path = cuda_build.build()
+    src = tmp_path / "use_ep.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include <string.h>
+#include "ep.h"
+int main(void) {
+  int64_t rows = 0, bytes = 0;
+  ep_status_t st = ep_get_buffer_size_hint(8, 256, 8, 7168, 1024, EP_FP8_E4M3, EP_LAYOUT_EXPERT_MAJOR, 128,
+                                           &rows, &bytes);
+  if (st != EP_OK || rows != 8192LL * 8 + 256LL * 127) return 1;
+  if (strcmp(ep_status_str(EP_ERR_CAPACITY), "EP_ERR_CAPACITY") != 0) return 2;
+  if (ep_handle_destroy(NULL) != EP_OK) return 3;
+  if (ep_handle_topk_idx_bits(NULL) != 0) return 4;
+  printf("ok %lld %lld\n", (long long)rows, (long long)bytes);
+  return 0;
+}
+''')
+    exe = tmp_path / "use_ep"
+    libdir = os.path.dirname(path)
+    cmd = ["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+           "-o", str(exe), "-L", libdir, "-l:" + os.path.basename(path), "-Wl,-rpath," + libdir]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0 and r.stdout.startswith("ok "), (r.returncode, r.stdout, r.stderr)
