@@ -2,10 +2,9 @@
 // + dispatch, and low_latency_dispatch, of "DeepEP 要約" (stakiran.github.io)
 // section 3).
 //
-// One persistent block per SM owns a contiguous run of tokens.  Its producer
-// warp starts streaming those tokens' rows into the shared-memory stage ring
-// at once -- the rows do not depend on the routing.  Meanwhile the consumer
-// warps rank the block's tokens:
+// One persistent block per SM: a producer warp and NC consumer warps.
+//
+// Routing.  Each block owns a contiguous run of tokens and ranks them:
 //   normal       -- per (token, destination rank): one lane per token, the
 //                   token's ranks as a 64-bit mask (R <= 64), one ballot per
 //                   distinct rank in a 32-token batch; expert counts by
@@ -13,24 +12,30 @@
 //   low latency / expert-major -- per (token, k) entry and expert:
 //                   __match_any_sync within a 32-entry batch, per-warp running
 //                   counts in shared memory.
-// Each block publishes its counts, all blocks meet at one bounded grid
+// Each block writes its counts (uint16), all blocks meet at one bounded grid
 // barrier (co-residency guaranteed by the cooperative launch), and each block
-// sums its predecessors' counts into exclusive prefixes, writes its tokens'
-// destinations and publishes them.  The row movement is not tied to the
-// routing's token ranges: the producer warps claim tokens in pairs from one
-// global counter from the first instruction on, so an SM that moves rows
-// faster takes more of them (the SMs of one GB300 do not all stream at the
-// same rate); a consumer reads a claimed token's destinations from global
-// memory once the owning block has published them, then quantises / stores
-// the row exactly as k_scatter does.  Per-expert totals, which nothing waits
-// for, are formed after the rows.  Rows and slots come out identical to the separate
-// routing kernels: (source rank, token) order per rank, (source rank, token,
-// k) order per expert.  The expert-major ("GEMM") layout of the V2 release
-// notes in "DeepSeek công bố thư viện mã nguồn mở DeepEP ..."
-// (vi.news.hada.io, "Những thay đổi chính của bản phát hành V2") packs those
-// per-expert slots one expert after another, each expert's group starting at
-// a multiple of the alignment; every block forms the group offsets itself
-// from the totals.
+// sums its predecessors' counts into exclusive prefixes.  Per-entry batches of
+// at most kFusedRedundantEntries entries skip the barrier: every block counts
+// every entry itself.  The block then writes its tokens' destinations and
+// publishes them (a per-block word set to the launch's generation + 1).
+//
+// Rows.  The row movement is not tied to the routing's token runs: from the
+// first instruction on, the producer claims tokens two at a time from one
+// global counter and streams their rows into the shared-memory stage ring (the
+// rows do not depend on the routing), so an SM that moves rows faster takes
+// more of them (the SMs of one GB300 do not all stream at the same rate).  A
+// consumer reads a claimed token's destinations from global memory once the
+// owning block has published them, then quantises / stores the row exactly as
+// k_scatter does.  Per-expert totals, which nothing waits for, are formed
+// after the rows.
+//
+// Rows and slots come out identical to the separate routing kernels: (source
+// rank, token) order per rank, (source rank, token, k) order per expert.  The
+// expert-major ("GEMM") layout of the V2 release notes in "DeepSeek công bố
+// thư viện mã nguồn mở DeepEP ..." (vi.news.hada.io, "Những thay đổi chính của
+// bản phát hành V2") packs those per-expert slots one expert after another,
+// each expert's group starting at a multiple of the alignment; every block
+// forms the group offsets itself from the totals.
 #include <climits>
 
 #include "ep_internal.h"
@@ -53,7 +58,7 @@ __device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
 }
 
 // Grid-wide barrier among the consumer warps of all blocks.  Word 0 counts
-// arrivals, word 1 is the generation, which thread 32 read (into g) when the
+// arrivals, word 1 is the generation, which the block read (into g) when the
 // kernel started: it cannot change before every block, this one included,
 // has arrived.  The block's writes are ordered before thread 32's fence by the
 // block barrier, the fence before its arrival; the last arrival releases the

@@ -79,7 +79,7 @@ def em_path(R, E, k, H, idx, w, x, fp8, align, y=None, num_sms=0, handle=None, c
 
 
 @pytest.mark.parametrize("name,align", [("tiny_bf16", 1), ("v3_ep8", 128), ("v3_ep8_group_limited", 64),
-                                        ("ll_decode_ep8", 8)])
+                                        ("ll_decode_ep8", 8), ("large_ep64_bwd", 32)])
 def test_em_workloads(name, align):
     w_ = wl.WORKLOADS[name]
     x, idx, wts = wl.make_inputs(w_)
