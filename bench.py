@@ -52,8 +52,8 @@ KERNEL_SOURCES = {"k_combine<normal>": ["combine.cu", "device_common.cuh", "ep_i
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
 # ncu capture of the V3-shaped workload, keyed by the kernel's source digest:
 # a kernel whose sources changed since its capture reports traffic = null.
-MEASURED_TRAFFIC = {"k_combine<normal>": ("6ce805801263a60e", 712687616),
-                    "k_route_scatter<fp8>": ("1094c7c56ae9464e", 382835456)}
+MEASURED_TRAFFIC = {"k_combine<normal>": ("c47023ae3ba5a3c4", 712500480),
+                    "k_route_scatter<fp8>": ("5fbf02e82124ee94", 382585088)}
 
 
 def kernel_digest(kernel: str) -> str:
@@ -676,6 +676,14 @@ def main():
     if graph_ms is not None and graph_ms < total_ms:
         total_ms, timed = graph_ms, "cuda_graph"
     per_op = time_ops(step, min(args.steps, 300), stream)
+    # the same ops on fewer SMs, for context (the pages let the caller bound
+    # the SMs the kernels occupy)
+    sweep = {}
+    for n in (24, 64):
+        step.num_sms = n
+        ts = time_ops(step, min(args.steps, 50), stream)
+        sweep[str(n)] = {name: round(statistics.median(v) * 1e3, 2) for name, v in ts.items()}
+    step.num_sms = args.num_sms
     status = step.h.get_device_status()
     if status != ep.EP_OK:
         raise RuntimeError(f"device status after the timed steps: {ep.status_str(status)}")
@@ -697,6 +705,7 @@ def main():
         mean_ms = statistics.fmean(ts)
         ops[name] = {
             "us": round(mean_ms * 1e3, 2),
+            "us_median": round(statistics.median(ts) * 1e3, 2),
             "us_p10": round(float(np.percentile(ts, 10)) * 1e3, 2),
             "us_p90": round(float(np.percentile(ts, 90)) * 1e3, 2),
             "logical_gbs": round(step.sizes.logical[name] / (mean_ms / 1e3) / 1e9, 1),
@@ -738,6 +747,7 @@ def main():
         "gpu_launches": len(OPS) * args.steps,
         "clocks": clocks,
     }
+    line["num_sms_sweep_us_median"] = sweep
     nxt = NextOps(step)
     line["next_ops"] = nxt.time(min(args.steps, 100), stream, peak)
     status = step.h.get_device_status()

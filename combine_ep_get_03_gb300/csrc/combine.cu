@@ -18,8 +18,9 @@
 //                entries in ascending expert id, from +0.0 with RN adds.
 //
 // HBM-bound gather-reduce.  Two blocks per SM (at most 128 registers a
-// thread): the e4m3 variant, which needs the most registers, is latency-bound
-// with one.  Work is split into (token, 1024-channel part)
+// thread), three for the e4m3 input (at most 85): its dequantisation makes it
+// latency-bound with fewer warps (148 us with one block, 101.6 with two, 92.9
+// with three on the V3 shape).  Work is split into (token, 1024-channel part)
 // items dealt round-robin to the warps of a persistent grid, so the last
 // round leaves few warps idle.  A warp takes a part one slab at a time (512
 // bf16 or 1024 e4m3 channels) and requests every source row of the slab
@@ -62,7 +63,7 @@ __device__ __forceinline__ void add_scaled2(float& a0, float& a1, float p0, floa
 }
 
 template <int kSrc, bool kFP8>
-__global__ void __launch_bounds__(kCombineThreads, 2) k_combine(CombineArgs a) {
+__global__ void __launch_bounds__(kCombineThreads, kFP8 ? 3 : 2) k_combine(CombineArgs a) {
   extern __shared__ int base_smem[];  // rank_offset [R+1] or expert_offset [E+1]
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -144,9 +145,9 @@ __global__ void __launch_bounds__(kCombineThreads, 2) k_combine(CombineArgs a) {
       for (int c = 0; c < kChunks; ++c)
 #pragma unroll
         for (int i = 0; i < kLaneCh; ++i) acc[c][i] = 0.0f;
-      // sources loaded together: e4m3 rows take half the batch (fewer
-      // registers, so two blocks fit an SM; 16 channels per chunk already)
-      constexpr int kBatch = kFP8 ? kMaxSrc / 2 : kMaxSrc;
+      // sources loaded together: e4m3 rows two at a time (16 channels per
+      // chunk already), so that three blocks fit an SM
+      constexpr int kBatch = kFP8 ? 2 : kMaxSrc;
       for (int sb = 0; sb < n; sb += kBatch) {
         uint4 v[kBatch][kChunks];
         float sc[kBatch][kChunks];
