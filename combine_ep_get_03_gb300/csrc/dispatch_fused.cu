@@ -57,32 +57,30 @@ __device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" : : "l"(p), "r"(v) : "memory");
 }
 
-// Grid-wide barrier among the consumer warps of all blocks.  Word 0 counts
-// arrivals, word 1 is the generation, which the block read (into g) when the
-// kernel started: it cannot change before every block, this one included,
-// has arrived.  The block's writes are ordered before thread 32's fence by the
-// block barrier, the fence before its arrival; the last arrival releases the
-// others by bumping the generation, then resets the count for the next launch
-// (nothing reads it again in this one).  Bounded: gives up after kSpinLimit
-// polls (latched kErrTimeout).
-__device__ inline void grid_sync(unsigned* words, unsigned g, unsigned nblocks, int* err, int nthreads) {
+__device__ __forceinline__ void red_release_add_u32(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" : : "l"(p), "r"(v) : "memory");
+}
+
+// Grid-wide barrier among the consumer warps of all blocks, on word 0 (the
+// arrival count, zero when the launch starts).  The block's writes are ordered
+// before thread 32's fence by the block barrier, the fence before its
+// releasing arrival; every block then polls the count itself until all nblocks
+// have arrived, so the last arrival is seen one L2 round trip after it lands.
+// The last block to finish the kernel resets the count (every block has passed
+// the barrier by then).  Bounded: gives up after kSpinLimit polls (latched
+// kErrTimeout).
+__device__ inline void grid_sync(unsigned* words, unsigned nblocks, int* err, int nthreads) {
   consumer_sync(nthreads);
   if (threadIdx.x == 32) {
     __threadfence();
-    const unsigned arrived = atomicAdd(words, 1u);
-    if (arrived == nblocks - 1) {
-      __threadfence();
-      st_release_u32(words + 1, g + 1);
-      atomicExch(words, 0u);
-    } else {
-      int it = 0;
-      while (ld_acquire_u32(words + 1) == g) {
-        if (++it > kSpinLimit) {
-          latch_error(err, kErrTimeout);
-          break;
-        }
-        if (it > 16) __nanosleep(64);
+    red_release_add_u32(words, 1u);
+    int it = 0;
+    while (ld_acquire_u32(words) < nblocks) {
+      if (++it > kSpinLimit) {
+        latch_error(err, kErrTimeout);
+        break;
       }
+      if (it > 16) __nanosleep(32);
     }
     __threadfence();
   }
@@ -451,7 +449,7 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
 
   // ---------------------------------------------------------------- phase 2: prefixes over blocks
   const bool barrier = !(kLL && a.redundant);
-  if (barrier) grid_sync(a.barrier, gen, static_cast<unsigned>(nb), a.err, nct);
+  if (barrier) grid_sync(a.barrier, static_cast<unsigned>(nb), a.err, nct);
   else consumer_sync(nct);
   const int ld = agg_ld(kLL ? E : R + E);
   if (!kLL) {
@@ -702,13 +700,14 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
   __syncwarp();
   // the last block to finish resets the claim counter for the next launch
   // (every claim of every block has returned by the time it counts itself)
-  // (and, when there was no grid barrier, advances the generation that the
-  // "published" words of the next launch are compared with)
+  // and the grid barrier's count, and advances the generation that the
+  // "published" words of the next launch are compared with
   consumer_sync(nct);
   if (threadIdx.x == 32 && atomicAdd(a.barrier + kCtlDone, 1u) == static_cast<unsigned>(nb) - 1) {
     atomicExch(a.barrier + kCtlClaim, 0u);
     atomicExch(a.barrier + kCtlDone, 0u);
-    if (!barrier) atomicAdd(a.barrier + 1, 1u);
+    atomicExch(a.barrier, 0u);
+    atomicAdd(a.barrier + 1, 1u);
   }
 }
 

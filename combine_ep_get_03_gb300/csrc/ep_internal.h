@@ -97,10 +97,11 @@ int combine_threads();
 const void* combine_kernel(int src, bool fp8);
 
 // Control words shared by the row-moving kernels (the handle's
-// fused_barrier array): [0] grid-barrier arrivals, [1] grid-barrier
-// generation, [2] row-claim counter, [3] blocks finished (the last block
-// resets [2] and [3]), [4 + b] block b's "destinations published" word of
-// the fused kernel (= generation + 1 once written).
+// fused_barrier array): [0] grid-barrier arrivals, [1] launch generation,
+// [2] row-claim counter, [3] blocks finished, [4 + b] block b's "destinations
+// published" word of the fused kernel (= generation + 1 once written).  The
+// last block to finish a launch resets [0], [2], [3] and (fused kernel)
+// advances [1].
 constexpr int kCtlClaim = 2, kCtlDone = 3, kCtlPub = 4;
 constexpr int kClaimTokens = 2;  // tokens per claim
 
