@@ -387,29 +387,41 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
     for (int i = ct; i < NC * E; i += nct) cnt[i] = 0;
     consumer_sync(nct);
     int* cntw = cnt + cw * E;
-    for (int b0 = cw * ipw; b0 < min(NI, (cw + 1) * ipw); b0 += 32) {  // warp-uniform
-      const int i = b0 + lane;
-      const int tl = i >> a.kp_log2;
-      const int j = i & (kp - 1);
-      const bool in_blk = i < (cw + 1) * ipw && tl < n_own;
-      int e = -1;
-      if (in_blk && j < k) {
-        long long v = load_topk_id(a.topk_idx, static_cast<long long>(t_begin + tl) * k + j, a.ids32);
-        if (v < -1 || v >= E) {
-          latch_error(a.err, kErrBadExpert);
-          v = -1;
+    const int w_end = min(NI, (cw + 1) * ipw);
+    for (int g0 = cw * ipw; g0 < w_end; g0 += 8 * 32) {  // warp-uniform
+      // up to 8 batches of 32 entries: every id load in flight before the
+      // ranking, which runs batch by batch in order
+      int ev[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int i = g0 + q * 32 + lane;
+        const int tl = i >> a.kp_log2;
+        const int j = i & (kp - 1);
+        long long v = -1;
+        if (i < w_end && tl < n_own && j < k) {
+          v = load_topk_id(a.topk_idx, static_cast<long long>(t_begin + tl) * k + j, a.ids32);
+          if (v < -1 || v >= E) {
+            latch_error(a.err, kErrBadExpert);
+            v = -1;
+          }
         }
-        e = static_cast<int>(v);
+        ev[q] = static_cast<int>(v);
       }
-      const unsigned pe = __match_any_sync(kFullMask, e);
-      int le = 0;
-      if (e >= 0) le = cntw[e] + __popc(pe & lt);
-      __syncwarp();
-      if (e >= 0 && lane == __ffs(pe) - 1) cntw[e] += __popc(pe);
-      __syncwarp();
-      if (i < NI) {
-        item_e[i] = e;
-        item_slot[i] = le;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (g0 + q * 32 >= w_end) break;  // warp-uniform
+        const int i = g0 + q * 32 + lane;
+        const int e = ev[q];
+        const unsigned pe = __match_any_sync(kFullMask, e);
+        int le = 0;
+        if (e >= 0) le = cntw[e] + __popc(pe & lt);
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(pe) - 1) cntw[e] += __popc(pe);
+        __syncwarp();
+        if (i < NI) {
+          item_e[i] = e;
+          item_slot[i] = le;
+        }
       }
     }
     consumer_sync(nct);
