@@ -39,21 +39,32 @@ from combine_ep_get_03_gb300 import workloads as wl  # noqa: E402
 METRIC = "dispatch & combine logical GB/s and % of GB300 HBM roofline (V3 shape, 1 GPU)"
 UNIT = "GB/s"
 OPS = ["layout_dispatch_fp8", "combine", "dispatch_bf16_bwd", "combine_bwd", "ll_dispatch_fp8", "ll_combine"]
-KERNEL_OF = {"layout_dispatch_fp8": "k_route_scatter<fp8>", "combine": "k_combine<normal>",
+# the step of each workload (the workload recipes: tiny = BF16 dispatch;
+# decode = the low-latency pair; large-EP backward = forward + backward, no
+# low-latency pair)
+OPS_OF = {"tiny_bf16": ["layout_dispatch_bf16", "combine", "dispatch_bf16_bwd", "combine_bwd", "ll_dispatch_fp8",
+                        "ll_combine"],
+          "v3_ep8": OPS, "v3_ep8_group_limited": OPS,
+          "ll_decode_ep8": ["ll_dispatch_fp8", "ll_combine"],
+          "large_ep64_bwd": ["layout_dispatch_fp8", "combine", "dispatch_bf16_bwd", "combine_bwd"]}
+KERNEL_OF = {"layout_dispatch_fp8": "k_route_scatter<fp8>", "layout_dispatch_bf16": "k_route_scatter<bf16>",
+             "combine": "k_combine<normal>",
              "dispatch_bf16_bwd": "k_scatter<bf16>", "combine_bwd": "k_combine<normal>",
              "ll_dispatch_fp8": "k_route_scatter<fp8,ll>", "ll_combine": "k_combine<ll>"}
 KERNEL_SOURCES = {"k_combine<normal>": ["combine.cu", "device_common.cuh", "ep_internal.h"],
                   "k_combine<ll>": ["combine.cu", "device_common.cuh", "ep_internal.h"],
                   "k_route_scatter<fp8>": ["dispatch_fused.cu", "scatter_common.cuh", "device_common.cuh",
                                            "ep_internal.h"],
+                  "k_route_scatter<bf16>": ["dispatch_fused.cu", "scatter_common.cuh", "device_common.cuh",
+                                            "ep_internal.h"],
                   "k_route_scatter<fp8,ll>": ["dispatch_fused.cu", "scatter_common.cuh", "device_common.cuh",
                                               "ep_internal.h"],
                   "k_scatter<bf16>": ["scatter_tma.cu", "scatter_common.cuh", "device_common.cuh", "ep_internal.h"]}
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
 # ncu capture of the V3-shaped workload, keyed by the kernel's source digest:
 # a kernel whose sources changed since its capture reports traffic = null.
-MEASURED_TRAFFIC = {"k_combine<normal>": ("c47023ae3ba5a3c4", 712500480),
-                    "k_route_scatter<fp8>": ("5fbf02e82124ee94", 382585088)}
+MEASURED_TRAFFIC = {"k_combine<normal>": ("0e445e2318af3cb3", 713098240),
+                    "k_route_scatter<fp8>": ("4fcbffbbab9bd01c", 383064320)}
 
 
 def kernel_digest(kernel: str) -> str:
@@ -88,6 +99,7 @@ class Sizes:
         row16 = 2 * H           # bf16 row
         self.logical = {
             "layout_dispatch_fp8": P * row8,
+            "layout_dispatch_bf16": P * row16,
             "combine": P * row16,
             "dispatch_bf16_bwd": P * row16,
             "combine_bwd": P * row16,
@@ -99,6 +111,8 @@ class Sizes:
             # layout (ids in; int32 ids and the (rank, row) list out) + FP8 dispatch
             "layout_dispatch_fp8": (8 * T * k + 4 * T * k + dst) + (2 * T * H + P * row8 + P * (4 + 8 * k) + dst
                                                                     + 8 * T * k),
+            "layout_dispatch_bf16": (8 * T * k + 4 * T * k + dst) + (2 * T * H + P * row16 + P * (4 + 8 * k) + dst
+                                                                     + 8 * T * k),
             "combine": P * row16 + 2 * T * H + dst,
             "dispatch_bf16_bwd": 2 * T * H + P * row16 + dst,
             "combine_bwd": P * row16 + 2 * T * H + dst,
@@ -110,10 +124,13 @@ class Sizes:
 # ----------------------------------------------------------------- GPU arm
 
 class Step:
-    """Device buffers for one batch and the seven ABI calls of one step."""
+    """Device buffers for one batch and the ABI calls of one step (the
+    workload's op list, OPS_OF)."""
 
     def __init__(self, w: wl.Workload, rep: int, dev: torch.device, num_sms: int):
         self.w, self.dev, self.num_sms = w, dev, num_sms
+        self.names = OPS_OF.get(w.name, OPS)
+        ll = "ll_dispatch_fp8" in self.names
         T, H, k, E = w.T, w.H, w.k, w.E
         G = H // 128
         x, idx, wts = wl.make_inputs(w, rep=rep)
@@ -131,6 +148,8 @@ class Step:
             return (torch.randn(shape, generator=gen, device=dev) * sigma).to(torch.bfloat16)
 
         self.recv = torch.empty((P, H), dtype=torch.uint8, device=dev)
+        self.recv_bf = (torch.empty((P, H), dtype=torch.bfloat16, device=dev)
+                        if "layout_dispatch_bf16" in self.names else None)
         self.scales = torch.empty((P, G), dtype=torch.float32, device=dev)
         self.src = torch.empty(P, dtype=torch.int32, device=dev)
         self.ridx = torch.empty((P, k), dtype=torch.int32, device=dev)
@@ -141,20 +160,22 @@ class Step:
         self.grad_in = torch.empty((P, H), dtype=torch.bfloat16, device=dev)
         self.grad_recv = randn_bf16((P, H), 1e-2)
         self.grad_x = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-        self.ll_recv = torch.empty((E, self.M, H), dtype=torch.uint8, device=dev)
-        self.ll_scales = torch.empty((E, self.M, G), dtype=torch.float32, device=dev)
-        self.ll_src = torch.empty((E, self.M), dtype=torch.int32, device=dev)
-        self.ll_cnt = torch.empty(E, dtype=torch.int32, device=dev)
-        self.y_ll = torch.empty((E, self.M, H), dtype=torch.bfloat16, device=dev)
-        self.out_ll = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-        # expert outputs on the rows low-latency dispatch fills
-        self.h.low_latency_dispatch(self.x, self.idx, ep.EP_FP8_E4M3, self.ll_recv, self.ll_scales,
-                                    recv_src_info=self.ll_src, recv_count=self.ll_cnt)
-        self.counts = self.ll_cnt.cpu().numpy().astype(np.int64)
-        n_ll = int(self.counts.sum())
-        self.ll_rows = torch.from_numpy(np.concatenate(
-            [e * self.M + np.arange(c) for e, c in enumerate(self.counts)])).to(dev)
-        self.y_ll.view(-1, H)[self.ll_rows] = randn_bf16((n_ll, H), w.y_sigma)
+        n_ll = 0
+        if ll:
+            self.ll_recv = torch.empty((E, self.M, H), dtype=torch.uint8, device=dev)
+            self.ll_scales = torch.empty((E, self.M, G), dtype=torch.float32, device=dev)
+            self.ll_src = torch.empty((E, self.M), dtype=torch.int32, device=dev)
+            self.ll_cnt = torch.empty(E, dtype=torch.int32, device=dev)
+            self.y_ll = torch.empty((E, self.M, H), dtype=torch.bfloat16, device=dev)
+            self.out_ll = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+            # expert outputs on the rows low-latency dispatch fills
+            self.h.low_latency_dispatch(self.x, self.idx, ep.EP_FP8_E4M3, self.ll_recv, self.ll_scales,
+                                        recv_src_info=self.ll_src, recv_count=self.ll_cnt)
+            self.counts = self.ll_cnt.cpu().numpy().astype(np.int64)
+            n_ll = int(self.counts.sum())
+            self.ll_rows = torch.from_numpy(np.concatenate(
+                [e * self.M + np.arange(c) for e, c in enumerate(self.counts)])).to(dev)
+            self.y_ll.view(-1, H)[self.ll_rows] = randn_bf16((n_ll, H), w.y_sigma)
         self.sizes = Sizes(w, P, n_ll)
         torch.cuda.synchronize(dev)
         status = self.h.get_device_status()
@@ -163,9 +184,12 @@ class Step:
 
     def ops(self):
         h, n = self.h, self.num_sms
-        return [
+        every = [
             ("layout_dispatch_fp8", lambda: h.layout_and_dispatch(
                 self.idx, self.x, self.wts, ep.EP_FP8_E4M3, self.recv, self.scales, recv_src_idx=self.src,
+                recv_topk_idx=self.ridx, recv_topk_weights=self.rw, num_sms=n)),
+            ("layout_dispatch_bf16", lambda: h.layout_and_dispatch(
+                self.idx, self.x, self.wts, ep.EP_BF16, self.recv_bf, recv_src_idx=self.src,
                 recv_topk_idx=self.ridx, recv_topk_weights=self.rw, num_sms=n)),
             ("combine", lambda: h.combine(self.y, self.out, num_sms=n)),
             ("dispatch_bf16_bwd", lambda: h.dispatch(self.grad_out, None, ep.EP_BF16, self.grad_in, num_sms=n)),
@@ -175,6 +199,7 @@ class Step:
                                                                recv_count=self.ll_cnt, num_sms=n)),
             ("ll_combine", lambda: h.low_latency_combine(self.y_ll, self.wts, self.out_ll, num_sms=n)),
         ]
+        return [op for op in every if op[0] in self.names]
 
 
 class NextOps:
@@ -395,26 +420,38 @@ def e2e_steps(step: Step, K: int, stream: torch.cuda.Stream):
     each op waits for the copies of its own inputs.  The low-latency expert
     outputs arrive packed (one copy) and are placed into the [E][M][H] layout
     on the device once the host has read the step's per-expert counts."""
+    names = [n for n, _ in step.ops()]
+    need = {"x", "idx", "wts"}
+    if "combine" in names:
+        need.add("y")
+    if "dispatch_bf16_bwd" in names:
+        need.add("grad_out")
+    if "combine_bwd" in names:
+        need.add("grad_recv")
+    ll = "ll_combine" in names
     pin = {}
     for name in ("x", "idx", "wts", "y", "grad_out", "grad_recv"):
-        t = getattr(step, name)
-        pin[name] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-        pin[name].copy_(t)
+        if name in need:
+            t = getattr(step, name)
+            pin[name] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            pin[name].copy_(t)
     H, E, M = step.w.H, step.w.E, step.M
-    y_ll_packed = step.y_ll.view(-1, H)[step.ll_rows]
-    pin["y_ll"] = torch.empty(y_ll_packed.shape, dtype=y_ll_packed.dtype, pin_memory=True)
-    pin["y_ll"].copy_(y_ll_packed)
-    staging = torch.empty_like(y_ll_packed)
-    outs = {n: torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
-            for n in ("out", "grad_x", "out_ll")}
-    counts = torch.empty(E, dtype=torch.int32, pin_memory=True)
-    rows_pin = torch.empty(y_ll_packed.shape[0], dtype=torch.int64, pin_memory=True)
-    rows_dev = torch.empty(y_ll_packed.shape[0], dtype=torch.int64, device=step.dev)
-    h2d = sum(p.numel() * p.element_size() for p in pin.values()) + rows_pin.numel() * 8
-    d2h = sum(o.numel() * o.element_size() for o in outs.values()) + counts.numel() * 4
+    out_names = [n for n, op in (("out", "combine"), ("grad_x", "combine_bwd"), ("out_ll", "ll_combine"))
+                 if op in names]
+    outs = {n: torch.empty(step.x.shape, dtype=torch.bfloat16, pin_memory=True) for n in out_names}
+    if ll:
+        y_ll_packed = step.y_ll.view(-1, H)[step.ll_rows]
+        pin["y_ll"] = torch.empty(y_ll_packed.shape, dtype=y_ll_packed.dtype, pin_memory=True)
+        pin["y_ll"].copy_(y_ll_packed)
+        staging = torch.empty_like(y_ll_packed)
+        counts = torch.empty(E, dtype=torch.int32, pin_memory=True)
+        rows_pin = torch.empty(y_ll_packed.shape[0], dtype=torch.int64, pin_memory=True)
+        rows_dev = torch.empty(y_ll_packed.shape[0], dtype=torch.int64, device=step.dev)
+    h2d = sum(p.numel() * p.element_size() for p in pin.values()) + (rows_pin.numel() * 8 if ll else 0)
+    d2h = sum(o.numel() * o.element_size() for o in outs.values()) + (E * 4 if ll else 0)
     ops = dict(step.ops())
     cs = torch.cuda.Stream(step.dev)
-    ev = {n: torch.cuda.Event() for n in ("in", "y", "go", "gr", "yl", "out", "gx", "rows")}
+    ev = {n: torch.cuda.Event() for n in ("in", "y", "grad_out", "grad_recv", "yl", "out", "grad_x")}
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(K):
@@ -423,42 +460,41 @@ def e2e_steps(step: Step, K: int, stream: torch.cuda.Stream):
             for name in ("x", "idx", "wts"):
                 getattr(step, name).copy_(pin[name], non_blocking=True)
             ev["in"].record(cs)
-            step.y.copy_(pin["y"], non_blocking=True)
-            ev["y"].record(cs)
-            step.grad_out.copy_(pin["grad_out"], non_blocking=True)
-            ev["go"].record(cs)
-            step.grad_recv.copy_(pin["grad_recv"], non_blocking=True)
-            ev["gr"].record(cs)
-            staging.copy_(pin["y_ll"], non_blocking=True)
-            ev["yl"].record(cs)
+            for name in ("y", "grad_out", "grad_recv"):
+                if name in pin:
+                    getattr(step, name).copy_(pin[name], non_blocking=True)
+                    ev[name].record(cs)
+            if ll:
+                staging.copy_(pin["y_ll"], non_blocking=True)
+                ev["yl"].record(cs)
         stream.wait_event(ev["in"])
-        ops["layout_dispatch_fp8"]()
-        stream.wait_event(ev["y"])
-        ops["combine"]()
-        ev["out"].record(stream)
-        stream.wait_event(ev["go"])
-        ops["dispatch_bf16_bwd"]()
-        stream.wait_event(ev["gr"])
-        ops["combine_bwd"]()
-        ev["gx"].record(stream)
-        with torch.cuda.stream(cs):
-            cs.wait_event(ev["out"])
-            outs["out"].copy_(step.out, non_blocking=True)
-            cs.wait_event(ev["gx"])
-            outs["grad_x"].copy_(step.grad_x, non_blocking=True)
-        ops["ll_dispatch_fp8"]()
-        counts.copy_(step.ll_cnt, non_blocking=True)
-        stream.synchronize()
-        c = counts.numpy().astype(np.int64)
-        if int(c.sum()) != rows_pin.numel():
-            raise RuntimeError("low-latency counts changed between steps of one batch")
-        starts = np.repeat(np.arange(E, dtype=np.int64) * M - np.concatenate([[0], np.cumsum(c)[:-1]]), c)
-        rows_pin.numpy()[:] = starts + np.arange(c.sum(), dtype=np.int64)
-        rows_dev.copy_(rows_pin, non_blocking=True)
-        stream.wait_event(ev["yl"])
-        step.y_ll.view(-1, H).index_copy_(0, rows_dev, staging)
-        ops["ll_combine"]()
-        outs["out_ll"].copy_(step.out_ll, non_blocking=True)
+        for name in names:
+            if name == "combine":
+                stream.wait_event(ev["y"])
+            elif name == "dispatch_bf16_bwd":
+                stream.wait_event(ev["grad_out"])
+            elif name == "combine_bwd":
+                stream.wait_event(ev["grad_recv"])
+            elif name == "ll_combine":
+                counts.copy_(step.ll_cnt, non_blocking=True)
+                stream.synchronize()
+                c = counts.numpy().astype(np.int64)
+                if int(c.sum()) != rows_pin.numel():
+                    raise RuntimeError("low-latency counts changed between steps of one batch")
+                starts = np.repeat(np.arange(E, dtype=np.int64) * M - np.concatenate([[0], np.cumsum(c)[:-1]]), c)
+                rows_pin.numpy()[:] = starts + np.arange(c.sum(), dtype=np.int64)
+                rows_dev.copy_(rows_pin, non_blocking=True)
+                stream.wait_event(ev["yl"])
+                step.y_ll.view(-1, H).index_copy_(0, rows_dev, staging)
+            ops[name]()
+            if name in ("combine", "combine_bwd"):
+                key = "out" if name == "combine" else "grad_x"
+                ev[key].record(stream)
+                with torch.cuda.stream(cs):
+                    cs.wait_event(ev[key])
+                    outs[key].copy_(getattr(step, key), non_blocking=True)
+            elif name == "ll_combine":
+                outs["out_ll"].copy_(step.out_ll, non_blocking=True)
         stream.synchronize()
         cs.synchronize()
     dt = time.perf_counter() - t0
@@ -534,17 +570,21 @@ def ll_decode_latency(dev: torch.device, reps: int = 200):
 # ----------------------------------------------------------------- CPU (oracle) arm
 
 def oracle_step(w: wl.Workload, tpr_s: int, rep: int = 0):
-    """One oracle pass over a sample of the workload: the first tpr_s tokens
-    of every source rank.  Returns (seconds, logical bytes)."""
+    """One oracle pass of the workload's step over a sample of it: the first
+    tpr_s tokens of every source rank.  Returns (seconds, logical bytes)."""
     import oracle  # the CPU reference implementation (test infrastructure)
 
+    names = OPS_OF.get(w.name, OPS)
     x, idx, wts = wl.make_inputs(w, rep=rep)
     tpr = w.tokens_per_rank
     keep = np.concatenate([np.arange(s * tpr, s * tpr + tpr_s) for s in range(w.R)])
     x, idx, wts = x[keep], idx[keep], wts[keep]
     R, E, k, H = w.R, w.E, w.k, w.H
     T = R * tpr_s
-    M = T
+    # rows per expert for the low-latency layout: the sample's largest expert
+    # (the results do not depend on any larger capacity)
+    valid = idx[idx >= 0]
+    M = max(1, int(np.bincount(valid, minlength=E).max()) if valid.size else 1)
     g = wl.rng(w.seed + 300, rep)
     t0 = time.perf_counter()
     L = oracle.layout(R, E, k, idx)
@@ -554,22 +594,30 @@ def oracle_step(w: wl.Workload, tpr_s: int, rep: int = 0):
     grad_out = wl.normal_bf16(g, (T, H), 1e-2)
     grad_recv = wl.normal_bf16(g, (P, H), 1e-2)
     gen = time.perf_counter() - t_gen
-    oracle.dispatch(R, E, k, x, idx, wts, fp8=True)
-    oracle.combine(R, E, k, idx, y)
-    oracle.dispatch(R, E, k, grad_out, idx, wts, fp8=False)
-    oracle.combine(R, E, k, idx, grad_recv)
-    ll, _ = oracle.ll_dispatch(R, E, k, M, x, idx, fp8=True)
-    n_ll = int(ll["recv_count"].sum())
-    t_gen = time.perf_counter()
-    y_ll = np.zeros((E, M, H), np.uint16)
-    flat = np.concatenate([e * M + np.arange(c) for e, c in enumerate(ll["recv_count"])]).astype(np.int64)
-    y_ll.reshape(E * M, H)[flat] = wl.normal_bf16(g, (n_ll, H))
-    gen += time.perf_counter() - t_gen
-    oracle.ll_combine(R, E, k, M, idx, wts, y_ll)
+    n_ll = 0
+    for name in names:
+        if name in ("layout_dispatch_fp8", "layout_dispatch_bf16"):
+            oracle.dispatch(R, E, k, x, idx, wts, fp8=name.endswith("fp8"))
+        elif name == "combine":
+            oracle.combine(R, E, k, idx, y)
+        elif name == "dispatch_bf16_bwd":
+            oracle.dispatch(R, E, k, grad_out, idx, wts, fp8=False)
+        elif name == "combine_bwd":
+            oracle.combine(R, E, k, idx, grad_recv)
+        elif name == "ll_dispatch_fp8":
+            ll, _ = oracle.ll_dispatch(R, E, k, M, x, idx, fp8=True)
+            n_ll = int(ll["recv_count"].sum())
+        elif name == "ll_combine":
+            t_gen = time.perf_counter()
+            y_ll = np.zeros((E, M, H), np.uint16)
+            flat = np.concatenate([e * M + np.arange(c) for e, c in enumerate(ll["recv_count"])]).astype(np.int64)
+            y_ll.reshape(E * M, H)[flat] = wl.normal_bf16(g, (n_ll, H))
+            gen += time.perf_counter() - t_gen
+            oracle.ll_combine(R, E, k, M, idx, wts, y_ll)
     dt = time.perf_counter() - t0 - gen
     sw = wl.Workload("sample", T=T, R=R, H=H, E=E, k=k, routing=w.routing, fp8=True, seed=w.seed)
     sizes = Sizes(sw, P, n_ll)
-    return dt, sum(sizes.logical.values())
+    return dt, sum(sizes.logical[n] for n in names)
 
 
 def cpu_cores_used() -> int:
@@ -687,20 +735,20 @@ def main():
     status = step.h.get_device_status()
     if status != ep.EP_OK:
         raise RuntimeError(f"device status after the timed steps: {ep.status_str(status)}")
-    total_ms, units = reduce_time_units(total_ms, float(sum(step.sizes.logical.values())) * args.steps, dev, world)
+    step_bytes = float(sum(step.sizes.logical[n] for n in step.names))
+    total_ms, units = reduce_time_units(total_ms, step_bytes * args.steps, dev, world)
     value = units / (total_ms / 1e3) / 1e9
 
     # end to end with host buffers
     barrier()
     e2e_dt, h2d, d2h = e2e_steps(step, args.e2e_steps, stream)
-    e2e_dt, e2e_units = reduce_time_units(e2e_dt, float(sum(step.sizes.logical.values())) * args.e2e_steps, dev,
-                                          world)
+    e2e_dt, e2e_units = reduce_time_units(e2e_dt, step_bytes * args.e2e_steps, dev, world)
     e2e_value = e2e_units / e2e_dt / 1e9
 
     peak, peak_kind = load_peak()
     ops = {}
     kernel_time = {}
-    for name in OPS:
+    for name in step.names:
         ts = per_op[name]
         mean_ms = statistics.fmean(ts)
         ops[name] = {
@@ -715,7 +763,7 @@ def main():
         }
         kernel_time[KERNEL_OF[name]] = kernel_time.get(KERNEL_OF[name], 0.0) + mean_ms
     dom = max(kernel_time, key=kernel_time.get)
-    dom_ops = [n for n in OPS if KERNEL_OF[n] == dom]
+    dom_ops = [n for n in step.names if KERNEL_OF[n] == dom]
     dom_ms = statistics.fmean([statistics.fmean(per_op[n]) for n in dom_ops])
     dom_bytes = statistics.fmean([step.sizes.hbm[n] for n in dom_ops])
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
@@ -744,16 +792,18 @@ def main():
                      "algorithmic_bytes_per_launch": int(dom_bytes), "launches_per_step": len(dom_ops)},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps},
-        "gpu_launches": len(OPS) * args.steps,
+        "gpu_launches": len(step.names) * args.steps,
         "clocks": clocks,
     }
     line["num_sms_sweep_us_median"] = sweep
-    nxt = NextOps(step)
-    line["next_ops"] = nxt.time(min(args.steps, 100), stream, peak)
-    status = step.h.get_device_status()
-    if status != ep.EP_OK:
-        raise RuntimeError(f"device status after the next-row ops: {ep.status_str(status)}")
-    line["ll_decode"] = ll_decode_latency(dev)
+    if w.name in ("v3_ep8", "v3_ep8_group_limited"):
+        nxt = NextOps(step)
+        line["next_ops"] = nxt.time(min(args.steps, 100), stream, peak)
+        status = step.h.get_device_status()
+        if status != ep.EP_OK:
+            raise RuntimeError(f"device status after the next-row ops: {ep.status_str(status)}")
+    if w.name in ("v3_ep8", "ll_decode_ep8"):
+        line["ll_decode"] = ll_decode_latency(dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # whole-batch oracle steps until about 10 s of CPU work (at most 3)
         tpr_s = w.tokens_per_rank
