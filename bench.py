@@ -63,8 +63,8 @@ KERNEL_SOURCES = {"k_combine<normal>": ["combine.cu", "device_common.cuh", "ep_i
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
 # ncu capture of the V3-shaped workload, keyed by the kernel's source digest:
 # a kernel whose sources changed since its capture reports traffic = null.
-MEASURED_TRAFFIC = {"k_combine<normal>": ("0e445e2318af3cb3", 713098240),
-                    "k_route_scatter<fp8>": ("4fcbffbbab9bd01c", 383064320)}
+MEASURED_TRAFFIC = {"k_combine<normal>": ("3a60cd054542d910", 693020160),
+                    "k_route_scatter<fp8>": ("94b64fa270b5d03c", 382264320)}
 
 
 def kernel_digest(kernel: str) -> str:
@@ -412,6 +412,42 @@ def time_ops(step: Step, K: int, stream: torch.cuda.Stream):
     return {name: [ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(K)] for i, (name, _) in enumerate(ops)}
 
 
+def time_ops_graph(step: Step, K: int, stream: torch.cuda.Stream):
+    """Per-op device times as the headline step runs them: one CUDA graph
+    holding the whole step with an event-record node between every op
+    (events created with ``external=True`` become real record nodes of the
+    graph), replayed K times.  Each op's time is then its kernel's duration
+    plus the graph's node-to-node latency, without the stream launch path
+    that ``time_ops`` includes.  Returns {op: [ms]} or None if capture fails."""
+    ops = step.ops()
+    n = len(ops)
+    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n + 1)]
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(step.dev)
+    side.wait_stream(stream)
+    try:
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                ev[0].record()
+                for i, (_, fn) in enumerate(ops):
+                    fn()
+                    ev[i + 1].record()
+    except Exception:
+        torch.cuda.synchronize(step.dev)
+        return None
+    stream.wait_stream(side)
+    out = {name: [] for name, _ in ops}
+    for rep in range(K + 3):
+        with torch.cuda.stream(stream):
+            g.replay()
+        ev[-1].synchronize()
+        if rep < 3:
+            continue
+        for i, (name, _) in enumerate(ops):
+            out[name].append(ev[i].elapsed_time(ev[i + 1]))
+    return out
+
+
 def e2e_steps(step: Step, K: int, stream: torch.cuda.Stream):
     """The same step through the public API with host buffers: every input
     copied host->device from pinned memory and every combine output copied
@@ -724,6 +760,7 @@ def main():
     if graph_ms is not None and graph_ms < total_ms:
         total_ms, timed = graph_ms, "cuda_graph"
     per_op = time_ops(step, min(args.steps, 300), stream)
+    per_op_graph = time_ops_graph(step, min(args.steps, 300), stream) if timed == "cuda_graph" else None
     # the same ops on fewer SMs, for context (the pages let the caller bound
     # the SMs the kernels occupy)
     sweep = {}
@@ -761,10 +798,22 @@ def main():
             "hbm_frac": round(step.sizes.hbm[name] / (mean_ms / 1e3) / 1e9 / peak, 4),
             "tokens_per_s": round(w.T / (mean_ms / 1e3), 1),
         }
+        if per_op_graph is not None:
+            tg = per_op_graph[name]
+            gmean = statistics.fmean(tg)
+            ops[name]["graph"] = {
+                "us": round(gmean * 1e3, 2),
+                "us_median": round(statistics.median(tg) * 1e3, 2),
+                "hbm_gbs": round(step.sizes.hbm[name] / (gmean / 1e3) / 1e9, 1),
+                "hbm_frac": round(step.sizes.hbm[name] / (gmean / 1e3) / 1e9 / peak, 4),
+            }
         kernel_time[KERNEL_OF[name]] = kernel_time.get(KERNEL_OF[name], 0.0) + mean_ms
     dom = max(kernel_time, key=kernel_time.get)
     dom_ops = [n for n in step.names if KERNEL_OF[n] == dom]
-    dom_ms = statistics.fmean([statistics.fmean(per_op[n]) for n in dom_ops])
+    # the dominant kernel's launch duration, in the launch mode the headline
+    # step was timed in (graph replays when they were faster)
+    dom_src, dom_timing = (per_op_graph, "cuda_graph") if per_op_graph is not None else (per_op, "stream")
+    dom_ms = statistics.fmean([statistics.fmean(dom_src[n]) for n in dom_ops])
     dom_bytes = statistics.fmean([step.sizes.hbm[n] for n in dom_ops])
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     trafficd = MEASURED_TRAFFIC.get(dom)
@@ -789,7 +838,8 @@ def main():
         "ops": ops,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
-                     "algorithmic_bytes_per_launch": int(dom_bytes), "launches_per_step": len(dom_ops)},
+                     "algorithmic_bytes_per_launch": int(dom_bytes), "launches_per_step": len(dom_ops),
+                     "timing": dom_timing},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps},
         "gpu_launches": len(step.names) * args.steps,

@@ -24,7 +24,10 @@
 // items dealt round-robin to the warps of a persistent grid, so the last
 // round leaves few warps idle.  A warp takes a part one slab at a time (512
 // bf16 or 1024 e4m3 channels) and requests every source row of the slab
-// before summing any, so up to kMaxSrc x 1 KB is in flight per warp.
+// before summing any, so up to kMaxSrc x 1 KB is in flight per warp; for
+// bf16 sources it first asks L2 for the rest of each source's part (a bulk
+// prefetch), which keeps tokens with few sources from starving HBM (combine
+// 102.4 -> 99.3 us on the group-limited V3 shape, unchanged on uniform V3).
 #include <climits>
 
 #include "device_common.cuh"
@@ -139,6 +142,16 @@ __global__ void __launch_bounds__(kCombineThreads, kFP8 ? 3 : 2) k_combine(Combi
     uint16_t* out = a.out + static_cast<size_t>(t) * a.H;
     const int h_end = min(a.H, (part + 1) * kPartChannels);
     constexpr int kLaneCh = kFP8 ? 16 : 8;  // channels per 16-byte chunk
+    constexpr int kSlab = 32 * kChunks * kLaneCh;
+    if (!kFP8 && part * kPartChannels + kSlab < h_end && lane < n) {
+      // bf16 sources: lane s asks L2 for the rest of the s-th source row's
+      // part while the first slab streams in (one bulk prefetch: 16-byte
+      // aligned, since y is and H is a multiple of 128), so a token with few
+      // sources still keeps enough bytes in flight
+      const uint16_t* yb = static_cast<const uint16_t*>(a.y);
+      const int h1 = part * kPartChannels + kSlab;
+      prefetch_l2_bulk(yb + srow * a.H + h1, static_cast<uint32_t>(h_end - h1) * 2u);
+    }
     for (int h0 = part * kPartChannels; h0 < h_end; h0 += 32 * kChunks * kLaneCh) {
       float acc[kChunks][kLaneCh];
 #pragma unroll

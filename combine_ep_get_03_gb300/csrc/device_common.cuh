@@ -41,6 +41,12 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
   return v;
 }
 
+// Asks L2 to fetch [p, p + bytes) (p 16-byte aligned, bytes a multiple of
+// 16); nothing waits for it.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" : : "l"(p), "r"(bytes) : "memory");
+}
+
 // 16-byte store that is not kept in L1.
 __device__ __forceinline__ void st_na(void* p, const uint4& v) {
   asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1, %2, %3, %4};"
