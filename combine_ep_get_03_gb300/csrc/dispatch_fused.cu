@@ -23,7 +23,12 @@
 // first instruction on, the producer claims tokens two at a time from one
 // global counter and streams their rows into the shared-memory stage ring (the
 // rows do not depend on the routing), so an SM that moves rows faster takes
-// more of them (the SMs of one GB300 do not all stream at the same rate).  A
+// more of them (the SMs of one GB300 do not all stream at the same rate).  In
+// the rank-major mode it streams only the first kRouteStages rows before its
+// own block has published the routing: a full ring of row loads from every SM
+// queues ahead of the routing's dependent loads and delays it (V3 shape:
+// 88.3 -> 86.4 us).  The per-entry modes keep the full ring (their consumers
+// start with eight stores a row, and the cap cost them 1-2 us).  A
 // consumer reads a claimed token's destinations from global memory once the
 // owning block has published them, then quantises / stores the row exactly as
 // k_scatter does.  Per-expert totals, which nothing waits for, are formed
@@ -212,7 +217,7 @@ __host__ __device__ inline size_t fused_smem_bytes(int mode, bool fp8, int R, in
                                                    int nc, int ns, int H) {
   const size_t route = (fused_route_bytes(mode, R, E, kmax, kp, tpb, nc) + 127) & ~static_cast<size_t>(127);
   const size_t qb = static_cast<size_t>(H) + ((4 * static_cast<size_t>(H / 128) + 15) & ~15ull);
-  return route + 16 * static_cast<size_t>(ns) + ((4 * static_cast<size_t>(ns) + 4 + 15) & ~15ull) +
+  return route + 16 * static_cast<size_t>(ns) + 16 + ((4 * static_cast<size_t>(ns) + 4 + 15) & ~15ull) +
          static_cast<size_t>(ns) * 2 * H + (fp8 ? nc * qb : 0);
 }
 
@@ -263,7 +268,8 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
   unsigned char* sbase = smem + ((fused_route_bytes(kMode, R, E, kmax, kp, tpb, NC) + 127) & ~static_cast<size_t>(127));
   uint64_t* full = reinterpret_cast<uint64_t*>(sbase);
   uint64_t* empty = full + NS;
-  int* stage_tok = reinterpret_cast<int*>(empty + NS);  // token held by each stage (-1: no more)
+  uint64_t* routed = empty + NS;  // completes when this block has published its routing
+  int* stage_tok = reinterpret_cast<int*>(routed + 2);  // token held by each stage (-1: no more)
   unsigned* sh_gen = reinterpret_cast<unsigned*>(stage_tok + NS);
   unsigned char* stage0 = reinterpret_cast<unsigned char*>(stage_tok) + ((4 * NS + 4 + 15) & ~15);
   unsigned char* qbuf0 = stage0 + static_cast<size_t>(NS) * row_bytes;
@@ -274,6 +280,7 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
       mbar_init(full + s, 1);
       mbar_init(empty + s, 1);
     }
+    mbar_init(routed, 1);
     mbar_init_fence();
     // the grid barrier's generation: written last by the previous launch (a
     // relaxed load sees it), and it cannot change before this block arrives
@@ -284,8 +291,10 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
 
   if (warp == 0) {
     // producer: claims tokens kClaimTokens at a time (one claim ahead) and
-    // streams their rows into the stages from the first instruction on; when
-    // the claims run out it hands every consumer warp a "no more" stage
+    // streams their rows into the stages (rank-major: the first kRouteStages
+    // from the first instruction on, the rest once this block has published
+    // its routing); when the claims run out it hands every consumer warp a
+    // "no more" stage
     if (lane == 0) {
       unsigned* claim = a.barrier + kCtlClaim;
       int base = static_cast<int>(atomicAdd(claim, static_cast<unsigned>(kClaimTokens)));
@@ -295,6 +304,10 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
       while (ok && base < a.T) {
         for (int c = 0; c < kClaimTokens && base + c < a.T; ++c, ++i) {
           const int s = i % NS;
+          if (!kLL && i == kRouteStages && !mbar_wait(routed, 0u, a.err)) {
+            ok = false;
+            break;
+          }
           if (i >= NS && !mbar_wait(empty + s, static_cast<uint32_t>((i / NS - 1) & 1), a.err)) {
             ok = false;
             break;
@@ -557,6 +570,7 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
   if (threadIdx.x == 32) {  // this block's destinations are visible to every block
     __threadfence();
     st_release_u32(a.barrier + kCtlPub + b, gen + 1);
+    mbar_arrive(routed);  // the producer may stream past kRouteStages rows (rank-major)
   }
 
   // ---------------------------------------------------------------- phase 3: move the rows
