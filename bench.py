@@ -451,9 +451,12 @@ def time_ops_graph(step: Step, K: int, stream: torch.cuda.Stream):
 def e2e_steps(step: Step, K: int, stream: torch.cuda.Stream, passes: int = 1):
     """The same step through the public API with host buffers: every input
     copied host->device from pinned memory and every combine output copied
-    back, each step, inside the timed region.  The copies run on a second
-    stream so that they overlap the kernels, as a caller would arrange it;
-    each op waits for the copies of its own inputs.  The low-latency expert
+    back, each step, inside the timed region.  The copies run on two more
+    streams (host->device and device->host, which the link carries at the
+    same time) so that they overlap the kernels and each other, as a caller
+    would arrange it; each op waits for the copies of its own inputs, and a
+    step's copies wait only for the previous step to be done with the
+    buffers they overwrite.  The low-latency expert
     outputs arrive packed (one copy) and are placed into the [E][M][H] layout
     on the device once the host has read the step's per-expert counts.
     Returns the seconds of each of `passes` passes of K steps."""
@@ -487,14 +490,16 @@ def e2e_steps(step: Step, K: int, stream: torch.cuda.Stream, passes: int = 1):
     h2d = sum(p.numel() * p.element_size() for p in pin.values()) + (rows_pin.numel() * 8 if ll else 0)
     d2h = sum(o.numel() * o.element_size() for o in outs.values()) + (E * 4 if ll else 0)
     ops = dict(step.ops())
-    cs = torch.cuda.Stream(step.dev)
-    ev = {n: torch.cuda.Event() for n in ("in", "y", "grad_out", "grad_recv", "yl", "out", "grad_x")}
+    cs = torch.cuda.Stream(step.dev)  # host -> device copies
+    ds = torch.cuda.Stream(step.dev)  # device -> host copies (the link is full duplex)
+    ev = {n: torch.cuda.Event() for n in ("in", "y", "grad_out", "grad_recv", "yl", "out", "grad_x", "out_ll")}
     dts = []
     for _ in range(passes):  # several passes: the host link is shared with other work on the machine
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for _ in range(K):
             cs.wait_stream(stream)  # the previous step no longer reads the inputs
+            stream.wait_stream(ds)  # nor its outputs
             with torch.cuda.stream(cs):
                 for name in ("x", "idx", "wts"):
                     getattr(step, name).copy_(pin[name], non_blocking=True)
@@ -526,18 +531,21 @@ def e2e_steps(step: Step, K: int, stream: torch.cuda.Stream, passes: int = 1):
                     stream.wait_event(ev["yl"])
                     step.y_ll.view(-1, H).index_copy_(0, rows_dev, staging)
                 ops[name]()
-                if name in ("combine", "combine_bwd"):
-                    key = "out" if name == "combine" else "grad_x"
+                if name in ("combine", "combine_bwd", "ll_combine"):
+                    key = {"combine": "out", "combine_bwd": "grad_x", "ll_combine": "out_ll"}[name]
                     ev[key].record(stream)
-                    with torch.cuda.stream(cs):
-                        cs.wait_event(ev[key])
+                    with torch.cuda.stream(ds):
+                        ds.wait_event(ev[key])
                         outs[key].copy_(getattr(step, key), non_blocking=True)
-                elif name == "ll_combine":
-                    outs["out_ll"].copy_(step.out_ll, non_blocking=True)
-            stream.synchronize()
-            cs.synchronize()
+        stream.synchronize()
+        cs.synchronize()
+        ds.synchronize()
         dt = time.perf_counter() - t0
         dts.append(dt)
+    # the pipelined copies brought back what the kernels wrote
+    for key, o in outs.items():
+        if not torch.equal(o, getattr(step, key).cpu()):
+            raise RuntimeError(f"end-to-end output {key} differs from the device result")
     return dts, h2d, d2h
 
 
