@@ -63,8 +63,8 @@ KERNEL_SOURCES = {"k_combine<normal>": ["combine.cu", "device_common.cuh", "ep_i
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
 # ncu capture of the V3-shaped workload, keyed by the kernel's source digest:
 # a kernel whose sources changed since its capture reports traffic = null.
-MEASURED_TRAFFIC = {"k_combine<normal>": ("8055d009ca22b04f", 693141760),
-                    "k_route_scatter<fp8>": ("0e231f8e1c60ac7f", 382574336)}
+MEASURED_TRAFFIC = {"k_combine<normal>": ("fdc36da53b536ef0", 693240320),
+                    "k_route_scatter<fp8>": ("49346cb790ee62f7", 382927616)}
 
 
 def kernel_digest(kernel: str) -> str:
