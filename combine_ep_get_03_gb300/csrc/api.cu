@@ -59,6 +59,27 @@ struct ep_handle {
   int* host;
 };
 
+namespace ep {
+
+// A flag word that no code writes: the self-check's flag wait never sees its
+// epoch and gives up.
+__device__ unsigned long long g_never_set_flag;
+
+// One thread waits on the flag above, then on a fresh mbarrier that nobody
+// arrives at; both waits are the bounded ones of the real kernels.
+__global__ void k_wait_timeout_check(int* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  (void)flag_wait(&g_never_set_flag, 1u, 1u, err);
+  mbar_init(&bar, 1);
+  mbar_init_fence();
+  (void)mbar_wait(&bar, 0u, err);
+}
+
+void launch_wait_timeout_check(int* err, cudaStream_t stream) { k_wait_timeout_check<<<1, 32, 0, stream>>>(err); }
+
+}  // namespace ep
+
 namespace {
 
 using ep::RouteParams;
@@ -915,6 +936,14 @@ ep_status_t ep_handle_set_topk_idx_bits(ep_handle_t h, int bits) {
 }
 
 int ep_handle_topk_idx_bits(ep_handle_t h) { return !h ? 0 : h->ids32 ? 32 : 64; }
+
+ep_status_t ep_check_wait_timeout(ep_handle_t h, ep_stream_t stream) {
+  if (!h) return EP_ERR_INVALID_ARG;
+  ep_status_t st = check_device(h);
+  if (st != EP_OK) return st;
+  ep::launch_wait_timeout_check(h->err, reinterpret_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError(), "ep_check_wait_timeout launch");
+}
 
 ep_status_t ep_get_device_status(ep_handle_t h, ep_stream_t stream) {
   if (!h) return EP_ERR_INVALID_ARG;

@@ -62,6 +62,7 @@ def lib() -> ctypes.CDLL:
             L.ep_low_latency_dispatch.argtypes = [P, P, P, I, I, P, P, P, P, I, P]
             L.ep_low_latency_combine.argtypes = [P, P, P, P, I, P]
             L.ep_get_device_status.argtypes = [P, P]
+            L.ep_check_wait_timeout.argtypes = [P, P]
             L.ep_get_dispatch_layout_noalloc.argtypes = [I, I, I, P, I, P, P, P, P, P, P, P, P, P, P]
             L.ep_status_str.argtypes = [I]
             L.ep_status_str.restype = ctypes.c_char_p
@@ -70,7 +71,7 @@ def lib() -> ctypes.CDLL:
                       "ep_low_latency_combine", "ep_combine_ex", "ep_handle_set_topk_idx_bits",
                       "ep_em_layout_and_dispatch", "ep_em_dispatch", "ep_em_get_layout", "ep_em_combine",
                       "ep_get_buffer_size_hint",
-                      "ep_get_device_status", "ep_get_dispatch_layout_noalloc"):
+                      "ep_get_device_status", "ep_check_wait_timeout", "ep_get_dispatch_layout_noalloc"):
                 getattr(L, n).restype = I
             _lib = L
     return _lib
@@ -285,6 +286,12 @@ def ep_get_buffer_size_hint(num_ranks, num_experts, num_topk, hidden, max_tokens
 def ep_get_device_status(h, stream=None) -> int:
     """Synchronise, then return and clear the latched device status."""
     return lib().ep_get_device_status(h, _stream(stream))
+
+
+def ep_check_wait_timeout(h, stream=None) -> None:
+    """Enqueue the bounded-wait self-check (waits that cannot complete give
+    up and latch EP_ERR_TIMEOUT; read it with ep_get_device_status)."""
+    _check(lib().ep_check_wait_timeout(h, _stream(stream)), "ep_check_wait_timeout")
 
 
 def ep_get_dispatch_layout_noalloc(num_ranks, num_experts, num_topk, topk_idx, num_recv_tokens_per_rank,
@@ -518,3 +525,6 @@ class Handle:
 
     def get_device_status(self, stream=None):
         return ep_get_device_status(self.ptr, stream)
+
+    def check_wait_timeout(self, stream=None):
+        ep_check_wait_timeout(self.ptr, stream)

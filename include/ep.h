@@ -379,6 +379,19 @@ ep_status_t ep_get_dispatch_layout_noalloc(int num_ranks, int num_experts, int n
  * latched since the last call (EP_OK if none). */
 ep_status_t ep_get_device_status(ep_handle_t h, ep_stream_t stream);
 
+/* Self-check of the bounded waits (failure detection without a fault).
+ * Enqueues one small kernel whose waits cannot complete: a flag wait on a
+ * device word that nothing sets and an mbarrier wait with no arrivals, each
+ * through the same bounded wait as the routing and dispatch kernels.  Each
+ * gives up after its poll limit (about half a second apiece), latches
+ * EP_ERR_TIMEOUT in the handle and returns, so the kernel ends by itself
+ * and the context stays usable; ep_get_device_status() then returns
+ * EP_ERR_TIMEOUT (and, as after any timeout, resets the fused kernel's
+ * control words).  Writes nothing but the handle's status latch.
+ * Returns EP_ERR_INVALID_ARG for a NULL handle, EP_ERR_CUDA if the launch
+ * fails. */
+ep_status_t ep_check_wait_timeout(ep_handle_t h, ep_stream_t stream);
+
 /* Static, NUL-terminated name of a status. */
 const char* ep_status_str(ep_status_t s);
 

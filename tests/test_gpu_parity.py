@@ -293,6 +293,31 @@ def test_capacity_overflow_is_latched_and_in_bounds():
     h.close()
 
 
+def test_a_wait_that_cannot_complete_ends_with_a_timeout_status():
+    """Failure detection without a fault: waits on a word that nothing sets
+    and on an mbarrier with no arrivals give up after their poll limit, the
+    kernel returns, the handle reports EP_ERR_TIMEOUT once, and the handle
+    and context still compute correct results afterwards."""
+    import time
+
+    R, E, k, H, tpr = 4, 16, 2, 256, 32
+    idx, w, x = _edge_inputs(R, E, k, H, tpr, 0.0, 0.0, seed=8)
+    h = ep.Handle(R, E, k, H, tpr)
+    t0 = time.perf_counter()
+    h.check_wait_timeout()
+    st = h.get_device_status()
+    dt = time.perf_counter() - t0
+    assert st == ep.EP_ERR_TIMEOUT
+    assert dt < 30.0, f"the bounded waits took {dt:.1f} s"
+    assert h.get_device_status() == ep.EP_OK  # cleared
+    # the fused kernel's control words were reset and everything still works
+    y = wl.normal_bf16(wl.rng(9), (int(oracle.layout(R, E, k, idx)["rank_offset"][-1]), H))
+    fused_path(R, E, k, H, idx, w, x, fp8=True, y=y, handle=h)
+    ll_path(R, E, k, H, idx, w, x, fp8=True, y_seed=9, handle=h)
+    assert h.get_device_status() == ep.EP_OK
+    h.close()
+
+
 def test_argument_errors_are_synchronous():
     h = ep.Handle(4, 16, 2, 256, 8)
     with pytest.raises(ep.EPError) as e:
