@@ -145,6 +145,10 @@ RouteParams route_params(ep_handle* h, const void* topk_idx, int T, int CT,
   return p;
 }
 
+// Rank-major batches of at most this many (token, k) entries count every
+// token in every block instead of meeting at the fused kernel's grid barrier.
+constexpr long long kFusedRedundantRankEntries = 4096;
+
 int sms_for(const ep_handle* h, int num_sms) {
   return num_sms <= 0 ? h->num_sms : (num_sms < h->num_sms ? num_sms : h->num_sms);
 }
@@ -153,7 +157,7 @@ ep::FusedArgs fused_args(ep_handle* h, const void* topk_idx, const uint16_t* x, 
   ep::FusedArgs f{};
   f.topk_idx = topk_idx;
   f.ids32 = h->ids32;
-  f.redundant = static_cast<long long>(T) * h->k <= ep::kFusedRedundantEntries ? 1 : 0;  // per-entry modes only
+  f.redundant = static_cast<long long>(T) * h->k <= ep::kFusedRedundantEntries ? 1 : 0;  // rank-major: reset by the caller
   f.x = x;
   f.topk_weights = w;
   f.T = T;
@@ -518,6 +522,7 @@ ep_status_t ep_layout_and_dispatch(ep_handle_t h, const void* topk_idx, int T, c
                        recv_topk_weights, num_sms, stream);
   }
   ep::FusedArgs f = fused_args(h, topk_idx, static_cast<const uint16_t*>(x), topk_weights, T);
+  f.redundant = static_cast<long long>(T) * h->k <= kFusedRedundantRankEntries ? 1 : 0;
   f.agg = h->fused_agg;
   f.dst = h->dst;
   f.idx32 = h->idx32;

@@ -14,10 +14,13 @@
 //                   counts in shared memory.
 // Each block writes its counts (uint16), all blocks meet at one bounded grid
 // barrier (co-residency guaranteed by the cooperative launch), and each block
-// sums its predecessors' counts into exclusive prefixes.  Per-entry batches of
-// at most kFusedRedundantEntries entries skip the barrier: every block counts
-// every entry itself.  The block then writes its tokens' destinations and
-// publishes them (a per-block word set to the launch's generation + 1).
+// sums its predecessors' counts into exclusive prefixes.  Small batches skip
+// the barrier -- every block counts every entry itself -- in the per-entry
+// modes up to kFusedRedundantEntries entries, in the rank-major mode (its own
+// instantiation, kRedRanks, so that the large-batch code is untouched) up to
+// the host's smaller limit (tiny shape: 20.4 -> 16.2 us as graph replays).
+// The block then writes its tokens' destinations and publishes them (a
+// per-block word set to the launch's generation + 1).
 //
 // Rows.  The row movement is not tied to the routing's token runs: from the
 // first instruction on, the producer claims tokens two at a time from one
@@ -221,10 +224,12 @@ __host__ __device__ inline size_t fused_smem_bytes(int mode, bool fp8, int R, in
          static_cast<size_t>(ns) * 2 * H + (fp8 ? nc * qb : 0);
 }
 
-template <bool kFP8, int kMode>
+template <bool kFP8, int kMode, bool kRedRanks = false>
 __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_scatter(FusedArgs a, int NS) {
   constexpr bool kLL = kMode != kSrcRanks;        // per-entry routing (low latency, expert-major)
   constexpr bool kEM = kMode == kSrcExpertMajor;  // packed expert groups
+  // rank-major batch small enough for every block to count every token
+  static_assert(!kRedRanks || !kLL, "redundant rank counting is a rank-major variant");
   extern __shared__ __align__(128) unsigned char smem[];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -359,7 +364,7 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
             a.idx32[static_cast<size_t>(t) * k + j0 + j] = static_cast<int>(e);
             if (e >= 0) {
               m |= 1ull << (static_cast<int>(e) / a.El);
-              atomicAdd(hist + static_cast<int>(e), 1);
+              if (!kRedRanks) atomicAdd(hist + static_cast<int>(e), 1);
             }
           }
         }
@@ -391,9 +396,40 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
         cnt[w * R + col] = run;
         run += v;
       }
-      a.agg[static_cast<size_t>(b) * agg_ld(R + E) + col] = static_cast<uint16_t>(run);
+      if (!kRedRanks) a.agg[static_cast<size_t>(b) * agg_ld(R + E) + col] = static_cast<uint16_t>(run);
     }
-    for (int e = ct; e < E; e += nct) a.agg[static_cast<size_t>(b) * agg_ld(R + E) + R + e] = static_cast<uint16_t>(hist[e]);
+    if (!kRedRanks) {
+      for (int e = ct; e < E; e += nct) a.agg[static_cast<size_t>(b) * agg_ld(R + E) + R + e] = static_cast<uint16_t>(hist[e]);
+    } else {
+      // a small batch: every block counts every token itself -- its
+      // destination ranks (all tokens into tot, earlier ones into excl) and its
+      // experts (into hist, here the per-expert totals) -- instead of meeting
+      // the other blocks at the grid barrier
+      for (int i = ct; i <= R; i += nct) excl[i] = tot[i] = 0;
+      consumer_sync(nct);
+      for (int t = ct; t < a.T; t += nct) {
+        unsigned long long m = 0;
+        for (int j0 = 0; j0 < k; j0 += 8) {
+          long long v[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            v[j] = j0 + j < k ? load_topk_id(a.topk_idx, static_cast<long long>(t) * k + j0 + j, a.ids32) : -1;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (v[j] >= 0 && v[j] < E) {
+              m |= 1ull << (static_cast<int>(v[j]) / a.El);
+              atomicAdd(hist + v[j], 1);
+            }
+          }
+        }
+        while (m) {
+          const int r = __ffsll(static_cast<long long>(m)) - 1;
+          m &= m - 1;
+          atomicAdd(tot + r, 1);
+          if (t < t_begin) atomicAdd(excl + r, 1);
+        }
+      }
+    }
   } else {
     const int NI = tpb << a.kp_log2;
     const int ipw = (((NI + NC - 1) / NC) + 31) & ~31;
@@ -473,12 +509,12 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
   }
 
   // ---------------------------------------------------------------- phase 2: prefixes over blocks
-  const bool barrier = !(kLL && a.redundant);
+  const bool barrier = kLL ? !a.redundant : !kRedRanks;
   if (barrier) grid_sync(a.barrier, static_cast<unsigned>(nb), a.err, nct);
   else consumer_sync(nct);
   const int ld = agg_ld(kLL ? E : R + E);
   if (!kLL) {
-    column_sums_par(a.agg, ld, R, nb, b, excl, tot, nct, ct);
+    if (!kRedRanks) column_sums_par(a.agg, ld, R, nb, b, excl, tot, nct, ct);
     consumer_sync(nct);
     if (cw == 0) {  // exclusive scan of the rank totals -> region offsets
       const int v = lane < R ? tot[lane] : 0;
@@ -715,7 +751,7 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
   // per-expert totals (outputs only, nothing above waits for them): block b
   // forms the totals of experts e = b, b + nb, ...
   for (int e = b + ct * nb; !kEM && e < E; e += nct * nb) {
-    const int all = kLL && a.redundant ? etot[e] : column_total(a.agg, ld, (kLL ? 0 : R) + e, nb);
+    const int all = kRedRanks ? hist[e] : kLL && a.redundant ? etot[e] : column_total(a.agg, ld, (kLL ? 0 : R) + e, nb);
     if (kLL) {
       if (a.recv_count) a.recv_count[e] = min(all, a.M);
     } else {
@@ -769,8 +805,10 @@ void fused_config(int mode, bool fp8, int T, int R, int E, int k, int kmax, int 
 }
 
 cudaError_t configure_fused(size_t smem_limit) {
-  const void* ks[6] = {reinterpret_cast<const void*>(k_route_scatter<false, kSrcRanks>),
+  const void* ks[8] = {reinterpret_cast<const void*>(k_route_scatter<false, kSrcRanks>),
                        reinterpret_cast<const void*>(k_route_scatter<true, kSrcRanks>),
+                       reinterpret_cast<const void*>(k_route_scatter<false, kSrcRanks, true>),
+                       reinterpret_cast<const void*>(k_route_scatter<true, kSrcRanks, true>),
                        reinterpret_cast<const void*>(k_route_scatter<false, kSrcLowLatency>),
                        reinterpret_cast<const void*>(k_route_scatter<true, kSrcLowLatency>),
                        reinterpret_cast<const void*>(k_route_scatter<false, kSrcExpertMajor>),
@@ -804,6 +842,9 @@ cudaError_t launch_fused(const FusedArgs& a, bool fp8, int mode, int blocks, int
   if (mode == kSrcExpertMajor)
     return fp8 ? cudaLaunchKernelEx(&cfg, k_route_scatter<true, kSrcExpertMajor>, a, NS)
                : cudaLaunchKernelEx(&cfg, k_route_scatter<false, kSrcExpertMajor>, a, NS);
+  if (a.redundant)
+    return fp8 ? cudaLaunchKernelEx(&cfg, k_route_scatter<true, kSrcRanks, true>, a, NS)
+               : cudaLaunchKernelEx(&cfg, k_route_scatter<false, kSrcRanks, true>, a, NS);
   return fp8 ? cudaLaunchKernelEx(&cfg, k_route_scatter<true, kSrcRanks>, a, NS)
              : cudaLaunchKernelEx(&cfg, k_route_scatter<false, kSrcRanks>, a, NS);
 }

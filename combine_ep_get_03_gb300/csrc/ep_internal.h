@@ -157,7 +157,7 @@ constexpr long long kFusedRedundantEntries = 16384;
 struct FusedArgs {
   const void* topk_idx;        // [T][k] int64, or int32 if ids32
   int ids32;
-  int redundant;               // per-entry modes: count redundantly, no grid barrier
+  int redundant;               // small batch: every block counts every entry, no grid barrier
   const uint16_t* x;
   const float* topk_weights;
   int T, R, E, El, k, kp_log2, kmax, H, M;
