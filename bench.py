@@ -63,8 +63,8 @@ KERNEL_SOURCES = {"k_combine<normal>": ["combine.cu", "device_common.cuh", "ep_i
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
 # ncu capture of the V3-shaped workload, keyed by the kernel's source digest:
 # a kernel whose sources changed since its capture reports traffic = null.
-MEASURED_TRAFFIC = {"k_combine<normal>": ("fdc36da53b536ef0", 693240320),
-                    "k_route_scatter<fp8>": ("49346cb790ee62f7", 382927616)}
+MEASURED_TRAFFIC = {"k_combine<normal>": ("6b3e9b47a0f1b60f", 692994304),
+                    "k_route_scatter<fp8>": ("7fc34461a6be0307", 382441472)}
 
 
 def kernel_digest(kernel: str) -> str:
