@@ -244,6 +244,8 @@ class NextOps:
             "em_combine": self.n_em * 2 * H + 2 * T * H + 8 * T * k,
             "combine_fp8_input": P * row8 + 2 * T * H + dst,
             "combine_with_weights": P * 2 * H + P * 4 * k + 2 * T * H + 4 * T * k + dst,
+            # cached handle: the (rank, row) lists, int32 ids and weights read
+            "dispatch_fp8_cached": 2 * T * H + P * row8 + P * (4 + 8 * k) + dst + 8 * T * k,
         }
         self.logical = {
             "layout_dispatch_fp8_ids32": P * row8,
@@ -251,6 +253,7 @@ class NextOps:
             "em_combine": self.n_em * 2 * H,
             "combine_fp8_input": P * row8,
             "combine_with_weights": P * 2 * H,
+            "dispatch_fp8_cached": P * row8,
         }
         torch.cuda.synchronize(dev)
 
@@ -269,6 +272,9 @@ class NextOps:
             ("combine_fp8_input", lambda: s.h.combine_ex(s.recv, self.out8, y_scales=s.scales, num_sms=n)),
             ("combine_with_weights", lambda: s.h.combine_ex(s.y, s.out, recv_topk_weights=s.rw,
                                                             combined_topk_weights=self.cw, num_sms=n)),
+            ("dispatch_fp8_cached", lambda: s.h.dispatch(s.x, s.wts, ep.EP_FP8_E4M3, s.recv, s.scales,
+                                                         recv_src_idx=s.src, recv_topk_idx=s.ridx,
+                                                         recv_topk_weights=s.rw, num_sms=n)),
         ]
 
     def time(self, K: int, stream: torch.cuda.Stream, peak: float):
