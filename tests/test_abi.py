@@ -57,11 +57,12 @@ def test_argument_checks_precede_cuda(lib):
     assert create(4, 16, 2, 512, 8, None) == 1
     # NULL handles
     for name in ("ep_get_dispatch_layout", "ep_dispatch", "ep_combine", "ep_low_latency_dispatch",
-                 "ep_low_latency_combine", "ep_get_device_status", "ep_get_num_recv"):
+                 "ep_low_latency_combine", "ep_get_device_status", "ep_get_num_recv", "ep_check_wait_timeout"):
         fn = getattr(lib, name)
         fn.restype = ctypes.c_int
         nargs = {"ep_get_dispatch_layout": 7, "ep_dispatch": 12, "ep_combine": 6, "ep_low_latency_dispatch": 11,
-                 "ep_low_latency_combine": 6, "ep_get_device_status": 2, "ep_get_num_recv": 5}[name]
+                 "ep_low_latency_combine": 6, "ep_get_device_status": 2, "ep_get_num_recv": 5,
+                 "ep_check_wait_timeout": 2}[name]
         fn.argtypes = [ctypes.c_void_p] * nargs
         assert fn(*([None] * nargs)) == 1, name
     lib.ep_handle_destroy.argtypes = [ctypes.c_void_p]
