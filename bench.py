@@ -22,6 +22,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -623,9 +624,11 @@ def ll_decode_latency(dev: torch.device, reps: int = 200):
 
 # ----------------------------------------------------------------- CPU (oracle) arm
 
-def oracle_step(w: wl.Workload, tpr_s: int, rep: int = 0):
+def oracle_step(w: wl.Workload, tpr_s: int, rep: int = 0, threads=None):
     """One oracle pass of the workload's step over a sample of it: the first
-    tpr_s tokens of every source rank.  Returns (seconds, logical bytes)."""
+    tpr_s tokens of every source rank; `threads` = n runs the row-moving
+    steps' token loops on n host threads (byte-identical results).  Returns
+    (seconds, logical bytes)."""
     import oracle  # the CPU reference implementation (test infrastructure)
 
     names = OPS_OF.get(w.name, OPS)
@@ -651,15 +654,15 @@ def oracle_step(w: wl.Workload, tpr_s: int, rep: int = 0):
     n_ll = 0
     for name in names:
         if name in ("layout_dispatch_fp8", "layout_dispatch_bf16"):
-            oracle.dispatch(R, E, k, x, idx, wts, fp8=name.endswith("fp8"))
+            oracle.dispatch(R, E, k, x, idx, wts, fp8=name.endswith("fp8"), threads=threads)
         elif name == "combine":
-            oracle.combine(R, E, k, idx, y)
+            oracle.combine(R, E, k, idx, y, threads=threads)
         elif name == "dispatch_bf16_bwd":
-            oracle.dispatch(R, E, k, grad_out, idx, wts, fp8=False)
+            oracle.dispatch(R, E, k, grad_out, idx, wts, fp8=False, threads=threads)
         elif name == "combine_bwd":
-            oracle.combine(R, E, k, idx, grad_recv)
+            oracle.combine(R, E, k, idx, grad_recv, threads=threads)
         elif name == "ll_dispatch_fp8":
-            ll, _ = oracle.ll_dispatch(R, E, k, M, x, idx, fp8=True)
+            ll, _ = oracle.ll_dispatch(R, E, k, M, x, idx, fp8=True, threads=threads)
             n_ll = int(ll["recv_count"].sum())
         elif name == "ll_combine":
             t_gen = time.perf_counter()
@@ -667,46 +670,115 @@ def oracle_step(w: wl.Workload, tpr_s: int, rep: int = 0):
             flat = np.concatenate([e * M + np.arange(c) for e, c in enumerate(ll["recv_count"])]).astype(np.int64)
             y_ll.reshape(E * M, H)[flat] = wl.normal_bf16(g, (n_ll, H))
             gen += time.perf_counter() - t_gen
-            oracle.ll_combine(R, E, k, M, idx, wts, y_ll)
+            oracle.ll_combine(R, E, k, M, idx, wts, y_ll, threads=threads)
     dt = time.perf_counter() - t0 - gen
     sw = wl.Workload("sample", T=T, R=R, H=H, E=E, k=k, routing=w.routing, fp8=True, seed=w.seed)
     sizes = Sizes(sw, P, n_ll)
     return dt, sum(sizes.logical[n] for n in names)
 
 
-def cpu_cores_used() -> int:
-    return 1  # the oracle is single-threaded
+def host_cores() -> int:
+    """Host cores this process may run on: the oracle's thread count."""
+    import oracle
+    return oracle.threads_available()
+
+
+def cpu_model() -> str:
+    """The host CPU's name from /proc/cpuinfo ("model name"; on Arm hosts,
+    which print none, the implementer and part codes)."""
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ":" in ln:
+                    key, val = (p.strip() for p in ln.split(":", 1))
+                    fields.setdefault(key, val)
+    except OSError:
+        return platform.machine()
+    if "model name" in fields:
+        return fields["model name"]
+    parts = [f"{k} {fields[k]}" for k in ("CPU implementer", "CPU part", "CPU variant") if k in fields]
+    return f"{platform.machine()} " + ", ".join(parts) if parts else platform.machine()
+
+
+def cpu_leg(w: wl.Workload, budget_s: float = 10.0, max_steps: int = 3):
+    """Whole-batch oracle steps, single-threaded and on every host core, each
+    until about budget_s seconds of work (at most max_steps).  Returns the
+    cpu_baseline object: the all-core leg as value, the single-thread leg
+    beside it."""
+    n = host_cores()
+    legs = {}
+    for threads in (n, None):
+        dts, lb = [], 0
+        while len(dts) < max_steps and sum(dts) < budget_s:
+            dt, lb = oracle_step(w, w.tokens_per_rank, rep=len(dts), threads=threads)
+            dts.append(dt)
+        legs[threads] = (lb * len(dts) / sum(dts) / 1e9, len(dts), sum(dts))
+    v_all, n_all, s_all = legs[n]
+    v_one, n_one, s_one = legs[None]
+    return {"value": round(v_all, 4), "unit": UNIT, "cores": n, "kind": "oracle", "model": cpu_model(),
+            "sample": f"{n_all} whole step(s) over the {w.T}-token batch on {n} threads, {s_all:.1f} s",
+            "single_thread": {"value": round(v_one, 4), "unit": UNIT, "cores": 1,
+                              "sample": f"{n_one} whole step(s), {s_one:.1f} s"}}
+
+
+def step_config(w: wl.Workload, P: int, n_ll: int, num_sms: int, world: int) -> dict:
+    """The config object of both arms' JSON lines (same keys, same values)."""
+    return {"workload": w.name, "tokens": w.T, "ranks": w.R, "hidden": w.H, "experts": w.E, "topk": w.k,
+            "dispatch": "fp8 e4m3, 128-channel scales", "combine": "bf16",
+            "recv_rows": P, "ll_rows": n_ll,
+            "l2": "inputs larger than L2: a step touches ~3.4 GB and every buffer is evicted by the rest "
+                  "of the step before it is read again",
+            "num_sms": num_sms, "parallelism": f"replicas x{world}"}
+
+
+def workload_rows(w: wl.Workload):
+    """(P, N): the workload's rank-major receive rows and unmasked entries,
+    from its routing alone (the counts both arms move)."""
+    _, idx, _ = wl.make_inputs(w, rep=0)
+    R, El, k = w.R, w.E_l, w.k
+    valid = idx >= 0
+    ranks = np.where(valid, idx // El, -1)
+    P = sum(int(np.any(ranks == r, axis=1).sum()) for r in range(R))
+    n_ll = int(valid.sum()) if "ll_dispatch_fp8" in OPS_OF.get(w.name, OPS) else 0
+    return P, n_ll
 
 
 def run_reference(args, w):
-    """--impl reference: the oracle, as it stands, on the host cores."""
+    """--impl reference: the oracle, as it stands, on every host core (its
+    token loops split over threads; byte-identical to the single-threaded
+    definitions)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if world > 1 and rank != 0:
         return
+    threads = host_cores()
     budget_s = 150.0
     calib_tpr = 4
-    dt, _ = oracle_step(w, calib_tpr)
+    dt, _ = oracle_step(w, calib_tpr, threads=threads)
     per_tok = dt / calib_tpr
     tpr_s = int(max(1, min(w.tokens_per_rank, budget_s / max(1, args.steps + args.warmup) / max(per_tok, 1e-9))))
     for _ in range(args.warmup):
-        oracle_step(w, tpr_s)
+        oracle_step(w, tpr_s, threads=threads)
     times, logical = [], 0
     for s in range(args.steps):
-        dt, lb = oracle_step(w, tpr_s, rep=0)
+        dt, lb = oracle_step(w, tpr_s, rep=0, threads=threads)
         times.append(dt)
         logical = lb
     total = sum(times)
     value = logical * args.steps / total / 1e9
     sample = f"first {tpr_s} of {w.tokens_per_rank} tokens per source rank ({w.R * tpr_s} tokens) per step"
+    P, n_ll = workload_rows(w)
+    num_sms = args.num_sms or (torch.cuda.get_device_properties(0).multi_processor_count
+                               if torch.cuda.is_available() else 152)
+    config = step_config(w, P, n_ll, num_sms, max(world, 1))
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16/e4m3",
-        "data": "synthetic", "config": {"workload": w.name, "tokens": w.T, "ranks": w.R, "hidden": w.H,
-                                        "experts": w.E, "topk": w.k, "sample": sample},
-        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cpu_cores_used(), "kind": "oracle",
-                         "sample": sample},
+        "data": "synthetic", "config": config,
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "model": cpu_model(), "sample": sample},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -846,13 +918,8 @@ def main():
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16/e4m3", "data": "synthetic",
-        "config": {"workload": w.name, "tokens": w.T, "ranks": w.R, "hidden": w.H, "experts": w.E, "topk": w.k,
-                   "dispatch": "fp8 e4m3, 128-channel scales", "combine": "bf16",
-                   "recv_rows": step.sizes.P, "ll_rows": step.sizes.n_ll,
-                   "l2": "inputs larger than L2: a step touches ~3.4 GB and every buffer is evicted by the rest "
-                         "of the step before it is read again",
-                   "num_sms": args.num_sms or torch.cuda.get_device_properties(dev).multi_processor_count,
-                   "parallelism": f"replicas x{world}"},
+        "config": step_config(w, step.sizes.P, step.sizes.n_ll,
+                              args.num_sms or torch.cuda.get_device_properties(dev).multi_processor_count, world),
         "tokens_per_s": round(w.T * world / (total_ms / args.steps / 1e3), 1),
         "launch": {"timed": timed,
                    "ms_per_step_stream": round(stream_ms / args.steps, 4),
@@ -878,16 +945,8 @@ def main():
     if w.name in ("v3_ep8", "ll_decode_ep8"):
         line["ll_decode"] = ll_decode_latency(dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        # whole-batch oracle steps until about 10 s of CPU work (at most 3)
-        tpr_s = w.tokens_per_rank
-        dts, lb = [], 0
-        while len(dts) < 3 and sum(dts) < 10.0:
-            dt, lb = oracle_step(w, tpr_s, rep=len(dts))
-            dts.append(dt)
-        line["cpu_baseline"] = {"value": round(lb * len(dts) / sum(dts) / 1e9, 4), "unit": UNIT,
-                                "cores": cpu_cores_used(), "kind": "oracle",
-                                "sample": f"{len(dts)} whole step(s) over the {w.T}-token batch, "
-                                          f"{sum(dts):.1f} s of CPU time"}
+        # whole-batch oracle steps, on every host core and on one thread
+        line["cpu_baseline"] = cpu_leg(w)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -28,8 +28,8 @@ int g_smem_optin[kMaxDevices] = {};
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // Once per device, with that device current: the device address of the
-// scratch array (its host-side name is only a stand-in) and the opt-in
-// shared-memory limit.
+// scratch array (its host-side name is only a stand-in), the opt-in
+// shared-memory limit, and the layout kernel's limit set to it.
 ep_status_t device_setup(int dev, unsigned long long** scratch, int* smem_optin) {
   std::lock_guard<std::mutex> lock(g_setup_mutex);
   if (!g_scratch_ptr[dev]) {
@@ -42,6 +42,9 @@ ep_status_t device_setup(int dev, unsigned long long** scratch, int* smem_optin)
     }
     int optin = 0;
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    // the layout kernel's shared-memory limit: the opt-in maximum, the value
+    // handle creation also sets, so the two never lower it under each other
+    if (e == cudaSuccess) e = ep::configure_layout(static_cast<size_t>(optin));
     if (e != cudaSuccess) return EP_ERR_CUDA;
     g_scratch_ptr[dev] = static_cast<unsigned long long*>(p);
     g_smem_optin[dev] = optin;
@@ -107,7 +110,6 @@ extern "C" ep_status_t ep_get_dispatch_layout_noalloc(int R, int E, int k, const
   // fallback latch and the look-back words this call uses.  All-zero words
   // never count as published.
   cudaError_t e = cudaMemsetAsync(scratch, 0, sizeof(unsigned long long) * (kFlagBase + static_cast<size_t>(C) * NK), s);
-  if (e == cudaSuccess) e = ep::configure_layout(static_cast<size_t>(optin));
   if (e != cudaSuccess) return EP_ERR_CUDA;
 
   ep::RouteParams p;

@@ -300,8 +300,10 @@ def ep_get_dispatch_layout_noalloc(num_ranks, num_experts, num_topk, topk_idx, n
                                    device_status=None, stream=None) -> None:
     """The handle-free, allocation-free layout: every output is a caller tensor
     (see include/ep.h for shapes); the scan state lives in the library."""
-    T = topk_idx.shape[0]
     R, E, k = num_ranks, num_experts, num_topk
+    if not isinstance(topk_idx, torch.Tensor) or topk_idx.dim() != 2 or topk_idx.shape[1] != k:
+        raise ValueError(f"topk_idx must be a [T, {k}] tensor (num_topk columns)")
+    T = topk_idx.shape[0]
     kmax = min(k, R)
     for t, n, name in ((num_recv_tokens_per_rank, R, "num_recv_tokens_per_rank"),
                        (num_recv_tokens_per_expert, E, "num_recv_tokens_per_expert"),

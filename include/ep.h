@@ -335,11 +335,10 @@ ep_status_t ep_get_buffer_size_hint(int num_ranks, int num_experts, int num_topk
 /* ep_get_dispatch_layout_noalloc -- the same layout computation as
  * ep_get_dispatch_layout, for callers that cannot allocate device memory.
  * The pages have no counterpart to this call; it exists for this library's
- * users.  Some callers cannot call cudaMalloc at all: code that runs while a
- * CUDA stream capture is in progress, serving runtimes that hand all device
- * memory to their own allocator up front and forbid further allocations, and
- * plugin hosts that call in per request with no place to keep a handle (whose
- * creation allocates).  This entry point needs no handle and allocates
+ * users.  Some callers cannot call cudaMalloc at all: serving runtimes that
+ * hand all device memory to their own allocator up front and forbid further
+ * allocations, and plugin hosts that call in per request with no place to
+ * keep a handle (whose creation allocates).  This entry point needs no handle and allocates
  * nothing: every result goes to caller buffers, and the cross-block scan state
  * lives in a fixed 1 MiB array in the library's device memory, which every GPU
  * that loads the library holds until the process exits.
@@ -366,7 +365,9 @@ ep_status_t ep_get_buffer_size_hint(int num_ranks, int num_experts, int num_topk
  *      device_status dev int32 [1] or NULL: if given (zeroed by the caller),
  *      receives the first device-side status (EP_ERR_BAD_EXPERT,
  *      EP_ERR_TIMEOUT); if NULL such statuses are dropped.  Bad ids are
- *      treated as masked either way. */
+ *      treated as masked either way.  Always pass it: after a look-back
+ *      timeout the offsets may be partial, and without device_status nothing
+ *      tells the caller so. */
 ep_status_t ep_get_dispatch_layout_noalloc(int num_ranks, int num_experts, int num_topk,
                                            const int64_t* topk_idx, int num_tokens,
                                            int* num_tokens_per_rank, int* num_tokens_per_expert,

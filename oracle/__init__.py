@@ -8,7 +8,10 @@ package smoke check and the benchmark's CPU-baseline leg may import this
 module; the product path never does.  It shares no code with the CUDA
 library.
 
-Arrays are numpy; bf16 tensors travel as uint16 bit patterns.
+Arrays are numpy; bf16 tensors travel as uint16 bit patterns.  The
+row-moving steps take ``threads=n`` to run the same definitions with their
+token loop split over n host threads (``ep_oracle_threads.cpp``; results are
+byte-identical), which only the CPU-baseline timing uses.
 """
 from __future__ import annotations
 
@@ -22,8 +25,11 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "ep_oracle.cpp")
 _LIB_PATH = os.path.join(_HERE, "libep_oracle.so")
+_SRC_THREADS = os.path.join(_HERE, "ep_oracle_threads.cpp")
+_LIB_THREADS = os.path.join(_HERE, "libep_oracle_threads.so")
 _lock = threading.Lock()
 _lib = None
+_lib_threads = None
 
 OK, INVALID_ARG, CAPACITY, BAD_EXPERT = 0, 1, 3, 4
 
@@ -38,7 +44,23 @@ def build(force: bool = False) -> str:
                "-shared", "-o", tmp, _SRC]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB_PATH)
+    build_threads(force)
     return _LIB_PATH
+
+
+def build_threads(force: bool = False) -> str:
+    """Compile the multi-threaded copy (ep_oracle_threads.cpp, which includes
+    the oracle's own source and splits its token loops over std::threads)."""
+    deps = [_SRC, os.path.join(_HERE, "ep_oracle.h"), _SRC_THREADS]
+    if force or not os.path.exists(_LIB_THREADS) or os.path.getmtime(_LIB_THREADS) < max(
+        os.path.getmtime(d) for d in deps
+    ):
+        tmp = _LIB_THREADS + f".tmp{os.getpid()}"
+        cmd = ["g++", "-std=c++17", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-pthread",
+               "-shared", "-o", tmp, _SRC_THREADS]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_THREADS)
+    return _LIB_THREADS
 
 
 def _load():
@@ -71,6 +93,39 @@ def _load():
                 getattr(lib, name).restype = I
             _lib = lib
     return _lib
+
+
+def _load_threads():
+    global _lib_threads
+    with _lock:
+        if _lib_threads is None:
+            lib = ctypes.CDLL(build_threads())
+            P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+            lib.ref_threads_available.argtypes = []
+            lib.ref_threads_dispatch.argtypes = [I, I, I, I, I, I, I, P, P, P, I64, P, P, P, P, P]
+            lib.ref_threads_combine.argtypes = [I, I, I, I, I, I, P, P, I64, P]
+            lib.ref_threads_combine_ex.argtypes = [I, I, I, I, I, I, P, I, P, P, I64, P, P, P]
+            lib.ref_threads_ll_dispatch.argtypes = [I, I, I, I, I, I, I, I, P, P, P, P, P, P, P]
+            lib.ref_threads_ll_combine.argtypes = [I, I, I, I, I, I, I, P, P, P, P]
+            for name in ("ref_threads_available", "ref_threads_dispatch", "ref_threads_combine",
+                         "ref_threads_combine_ex", "ref_threads_ll_dispatch", "ref_threads_ll_combine"):
+                getattr(lib, name).restype = I
+            _lib_threads = lib
+    return _lib_threads
+
+
+def threads_available() -> int:
+    """Host cores this process may run on (sched_getaffinity)."""
+    return int(_load_threads().ref_threads_available())
+
+
+def _step(name, threads):
+    """The single-threaded oracle function, or (threads = n) its copy whose
+    token loop runs on n threads -- byte-identical results."""
+    if threads is None:
+        return getattr(_load(), "ref_" + name)
+    f = getattr(_load_threads(), "ref_threads_" + name)
+    return lambda *a: f(int(threads), *a)
 
 
 def _p(a):
@@ -147,7 +202,7 @@ def layout(R, E, k, topk_idx):
     return out
 
 
-def dispatch(R, E, k, x_bits, topk_idx, topk_weights, fp8, capacity_rows=None):
+def dispatch(R, E, k, x_bits, topk_idx, topk_weights, fp8, capacity_rows=None, threads=None):
     """Normal dispatch.  Returns (dict of outputs, status)."""
     x_bits = _c(x_bits, np.uint16)
     idx = _c(topk_idx, np.int64)
@@ -163,7 +218,7 @@ def dispatch(R, E, k, x_bits, topk_idx, topk_weights, fp8, capacity_rows=None):
         recv_topk_idx=np.full((rows, k), -7, np.int32),
         recv_topk_weights=np.full((rows, k), -7.0, np.float32),
     )
-    st = _check(_load().ref_dispatch(R, E, k, T, H, int(bool(fp8)), _p(x_bits), _p(idx), _p(w),
+    st = _check(_step("dispatch", threads)(R, E, k, T, H, int(bool(fp8)), _p(x_bits), _p(idx), _p(w),
                                      int(capacity_rows), _p(out["recv_x"]), _p(out["recv_scales"]),
                                      _p(out["recv_src_idx"]), _p(out["recv_topk_idx"]),
                                      _p(out["recv_topk_weights"])), allow=(OK, CAPACITY))
@@ -174,18 +229,18 @@ def dispatch(R, E, k, x_bits, topk_idx, topk_weights, fp8, capacity_rows=None):
     return out, st
 
 
-def combine(R, E, k, topk_idx, y_bits):
+def combine(R, E, k, topk_idx, y_bits, threads=None):
     """Normal combine: y (uint16 [rows, H]) -> out (uint16 [T, H])."""
     idx = _c(topk_idx, np.int64)
     y_bits = _c(y_bits, np.uint16)
     T = idx.shape[0]
     H = y_bits.shape[1]
     out = np.zeros((T, H), np.uint16)
-    _check(_load().ref_combine(R, E, k, T, H, _p(idx), _p(y_bits), y_bits.shape[0], _p(out)))
+    _check(_step("combine", threads)(R, E, k, T, H, _p(idx), _p(y_bits), y_bits.shape[0], _p(out)))
     return out
 
 
-def ll_dispatch(R, E, k, M, x_bits, topk_idx, fp8):
+def ll_dispatch(R, E, k, M, x_bits, topk_idx, fp8, threads=None):
     """Low-latency dispatch into [E, M, H].  Returns (dict, status)."""
     x_bits = _c(x_bits, np.uint16)
     idx = _c(topk_idx, np.int64)
@@ -197,14 +252,14 @@ def ll_dispatch(R, E, k, M, x_bits, topk_idx, fp8):
         recv_count=np.zeros(E, np.int32),
         slot=np.zeros((T, k), np.int32),
     )
-    st = _check(_load().ref_ll_dispatch(R, E, k, T, H, M, int(bool(fp8)), _p(x_bits), _p(idx),
+    st = _check(_step("ll_dispatch", threads)(R, E, k, T, H, M, int(bool(fp8)), _p(x_bits), _p(idx),
                                         _p(out["recv_x"]), _p(out["recv_scales"]),
                                         _p(out["recv_src_info"]), _p(out["recv_count"]),
                                         _p(out["slot"])), allow=(OK, CAPACITY))
     return out, st
 
 
-def ll_combine(R, E, k, M, topk_idx, topk_weights, y_bits):
+def ll_combine(R, E, k, M, topk_idx, topk_weights, y_bits, threads=None):
     """Low-latency combine: y (uint16 [E, M, H]) -> out (uint16 [T, H])."""
     idx = _c(topk_idx, np.int64)
     w = _c(topk_weights, np.float32)
@@ -212,11 +267,11 @@ def ll_combine(R, E, k, M, topk_idx, topk_weights, y_bits):
     T = idx.shape[0]
     H = y_bits.shape[-1]
     out = np.zeros((T, H), np.uint16)
-    _check(_load().ref_ll_combine(R, E, k, T, H, M, _p(idx), _p(w), _p(y_bits), _p(out)))
+    _check(_step("ll_combine", threads)(R, E, k, T, H, M, _p(idx), _p(w), _p(y_bits), _p(out)))
     return out
 
 
-def combine_ex(R, E, k, topk_idx, y, y_scales=None, recv_topk_weights=None):
+def combine_ex(R, E, k, topk_idx, y, y_scales=None, recv_topk_weights=None, threads=None):
     """Normal combine, general form.  y is uint16 bf16 bits [rows, H], or
     uint8 e4m3 bytes [rows, H] with fp32 y_scales [rows, H/128].  With
     recv_topk_weights [rows, k] the weights are summed back too.  Returns
@@ -230,7 +285,7 @@ def combine_ex(R, E, k, topk_idx, y, y_scales=None, recv_topk_weights=None):
     H = y.shape[1]
     out = np.zeros((T, H), np.uint16)
     cw = None if rw is None else np.zeros((T, k), np.float32)
-    _check(_load().ref_combine_ex(R, E, k, T, H, _p(idx), int(fp8), _p(y), _p(sc), y.shape[0], _p(rw),
+    _check(_step("combine_ex", threads)(R, E, k, T, H, _p(idx), int(fp8), _p(y), _p(sc), y.shape[0], _p(rw),
                                   _p(out), _p(cw)))
     return out, cw
 

@@ -64,3 +64,25 @@ def test_clock_slowdowns_are_reported():
 def test_no_samples_is_not_a_clock_reading():
     s = _sampler([]).summary()
     assert s["sm_mhz"] is None and s["samples"] == 0
+
+
+def test_reference_arm_rows_match_the_oracle_layout():
+    """The reference arm's config reports the same receive rows as the GPU
+    arm, whose rows come from the layout: check them against the oracle's."""
+    import oracle
+    from combine_ep_get_03_gb300 import workloads as wl
+
+    for name in ("tiny_bf16", "v3_ep8"):
+        w = wl.WORKLOADS[name]
+        _, idx, _ = wl.make_inputs(w, rep=0)
+        P, n_ll = bench.workload_rows(w)
+        assert P == int(oracle.layout(w.R, w.E, w.k, idx)["rank_offset"][-1])
+        has_ll = "ll_dispatch_fp8" in bench.OPS_OF.get(name, bench.OPS)
+        assert n_ll == (int((idx >= 0).sum()) if has_ll else 0)
+    cfg = bench.step_config(wl.WORKLOADS["v3_ep8"], 1, 2, 152, 1)
+    assert {"workload", "dispatch", "combine", "recv_rows", "ll_rows", "num_sms", "parallelism"} <= set(cfg)
+
+
+def test_cpu_model_and_cores_are_reported():
+    assert bench.cpu_model()
+    assert bench.host_cores() >= 1

@@ -140,3 +140,27 @@ def test_interleaved_paths_as_graph_replays(num_sms):
             p.check(name)
     assert h.get_device_status() == ep.EP_OK
     h.close()
+
+
+def test_a_smaller_handle_created_later_leaves_the_larger_one_working():
+    """Kernels whose shared memory grows with R + E (the R > 64 layout, the
+    low-latency routing fallback) keep working on a handle after a smaller
+    handle is created: the per-kernel shared-memory limit does not follow the
+    last handle's shape."""
+    from harness import check_layout, ll_path
+
+    R, k, H, tpr = 128, 8, 128, 8
+    T = R * tpr
+    big = ep.Handle(R, 1024, k, H, tpr)      # layout ~96 KB, low-latency routing ~91 KB of shared memory
+    small = ep.Handle(R, 128, k, H, tpr)     # ~60 KB and ~55 KB
+    for E, h in ((1024, big), (128, small), (1024, big)):
+        g = wl.rng(40 + E)
+        idx, w = wl.route_uniform(g, T, E, k)
+        x = wl.normal_bf16(g, (T, H))
+        check_layout(h, idx)
+        # one SM: too many (token, k) entries for the fused kernel, so the
+        # routing runs in the separate low-latency routing kernel
+        ll_path(R, E, k, H, idx, w, x, fp8=True, num_sms=1, handle=h)
+        assert h.get_device_status() == ep.EP_OK
+    small.close()
+    big.close()
