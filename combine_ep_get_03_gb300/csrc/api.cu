@@ -248,10 +248,6 @@ ep_status_t ep_handle_create(int R, int E, int k, int H, int max_tpr, ep_handle_
   }
   h->layout_cmax = R * ceil_div(max_tpr, h->layout_CT < ep::kLayoutTokenChunk ? h->layout_CT : ep::kLayoutTokenChunk);
   h->layout_tokens_smem = ep::layout_tokens_smem(R, E, ep::kLayoutTokenChunk, h->kmax);
-  if (R <= 64 && h->layout_tokens_smem > static_cast<size_t>(prop.sharedMemPerBlockOptin)) {
-    delete h;
-    return EP_ERR_INVALID_ARG;
-  }
   h->ll_cmax = R * ceil_div(max_tpr, h->ll_CT);
 
   // one device arena for all metadata
@@ -320,13 +316,15 @@ ep_status_t ep_handle_create(int R, int E, int k, int H, int max_tpr, ep_handle_
   h->smem_optin = optin;
   for (int f = 0; f < 2; ++f)
     for (int m = 0; m < 3; ++m) ep::scatter_config(H, R, E, f == 1, m, optin, &h->scatter_ns[f][m], &h->scatter_nc[f][m]);
-  // every kernel's dynamic shared-memory limit is set to the device's opt-in
-  // maximum, the same value for every handle: a per-handle size would let a
-  // later, smaller handle lower the limit under an earlier, larger one
-  if ((st = cuda_status(ep::configure_layout(optin), "configure_layout")) != EP_OK ||
-      (st = cuda_status(ep::configure_ll_dispatch(optin), "configure_ll_dispatch")) != EP_OK ||
-      (st = cuda_status(ep::configure_ll_route(optin), "configure_ll_route")) != EP_OK ||
-      (st = cuda_status(ep::configure_layout_tokens(optin), "configure_layout_tokens")) != EP_OK ||
+  // every kernel's dynamic shared-memory limit is set from the device's
+  // opt-in maximum, the same value for every handle (a per-handle size would
+  // let a later, smaller handle lower it under an earlier, larger one); a
+  // handle whose sizes do not fit under it is refused
+  if ((st = cuda_status(ep::configure_layout(h->layout_smem, optin), "configure_layout")) != EP_OK ||
+      (st = cuda_status(ep::configure_ll_dispatch(h->ll_smem, optin), "configure_ll_dispatch")) != EP_OK ||
+      (st = cuda_status(ep::configure_ll_route(h->ll_route_smem, optin), "configure_ll_route")) != EP_OK ||
+      (st = cuda_status(ep::configure_layout_tokens(R <= 64 ? h->layout_tokens_smem : 0, optin),
+                        "configure_layout_tokens")) != EP_OK ||
       (st = cuda_status(ep::configure_scatter(optin), "configure_scatter")) != EP_OK ||
       (st = cuda_status(ep::configure_fused(optin), "configure_fused")) != EP_OK) {
     ep_handle_destroy(h);

@@ -804,7 +804,7 @@ void fused_config(int mode, bool fp8, int T, int R, int E, int k, int kmax, int 
   if (*NS > 0) *blocks = nb;
 }
 
-cudaError_t configure_fused(size_t smem_limit) {
+cudaError_t configure_fused(size_t optin) {
   const void* ks[8] = {reinterpret_cast<const void*>(k_route_scatter<false, kSrcRanks>),
                        reinterpret_cast<const void*>(k_route_scatter<true, kSrcRanks>),
                        reinterpret_cast<const void*>(k_route_scatter<false, kSrcRanks, true>),
@@ -814,8 +814,7 @@ cudaError_t configure_fused(size_t smem_limit) {
                        reinterpret_cast<const void*>(k_route_scatter<false, kSrcExpertMajor>),
                        reinterpret_cast<const void*>(k_route_scatter<true, kSrcExpertMajor>)};
   for (const void* kk : ks) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_limit));
+    cudaError_t e = set_dynamic_smem_limit(kk, 0, optin);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -21,6 +21,21 @@ inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Dynamic shared-memory limit of a kernel: the device's opt-in maximum less
+// the kernel's static shared memory -- the same value whatever handle asks,
+// so no later call lowers it under an earlier one.  Fails (without touching
+// the attribute) if `needed` bytes do not fit under it; *limit (if given)
+// receives the limit.
+inline cudaError_t set_dynamic_smem_limit(const void* kernel, size_t needed, size_t optin, size_t* limit = nullptr) {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+  if (e != cudaSuccess) return e;
+  const size_t lim = optin > fa.sharedSizeBytes ? optin - fa.sharedSizeBytes : 0;
+  if (limit) *limit = lim;
+  if (needed > lim) return cudaErrorInvalidValue;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(lim));
+}
+
 struct RouteParams;  // routing.cuh
 
 struct LowLatencyOutPtrs {
@@ -42,12 +57,12 @@ struct LayoutOutPtrs {
 };
 
 void launch_layout(const RouteParams& p, const LayoutOutPtrs& out, size_t smem, cudaStream_t stream);
-cudaError_t configure_layout(size_t smem);
+cudaError_t configure_layout(size_t needed, size_t optin, size_t* limit = nullptr);
 // token-per-lane layout (R <= 64)
 constexpr int kLayoutTokenChunk = 256;
 void launch_layout_tokens(const RouteParams& p, const LayoutOutPtrs& out, cudaStream_t stream);
 size_t layout_tokens_smem(int R, int E, int CT, int kmax);
-cudaError_t configure_layout_tokens(size_t smem);
+cudaError_t configure_layout_tokens(size_t needed, size_t optin);
 
 // Normal dispatch: one warp per token, persistent grid.
 struct DispatchArgs {
@@ -145,7 +160,7 @@ struct ScatterArgs {
 // rows are too long for the bulk-copy staging).
 void scatter_config(int H, int R, int E, bool fp8, int mode, size_t smem_limit, int* NS, int* NC);
 size_t scatter_smem_bytes(int H, int R, int E, bool fp8, int mode, int NS, int NC);
-cudaError_t configure_scatter(size_t smem_limit);
+cudaError_t configure_scatter(size_t optin);
 void launch_scatter(const ScatterArgs& a, bool fp8, int mode, int blocks, int NS, int NC, cudaStream_t stream);
 
 // Fused routing + dispatch (cooperative launch, one block per SM).
@@ -193,12 +208,12 @@ struct FusedArgs {
 };
 void fused_config(int mode, bool fp8, int T, int R, int E, int k, int kmax, int H, int sms, size_t smem_limit,
                   int* blocks, int* NS, int* NC);
-cudaError_t configure_fused(size_t smem_limit);
+cudaError_t configure_fused(size_t optin);
 cudaError_t launch_fused(const FusedArgs& a, bool fp8, int mode, int blocks, int NS, int NC, cudaStream_t stream);
 
 // Low-latency routing only (slots, counts); the rows move with k_scatter.
 void launch_ll_route(const RouteParams& p, const LowLatencyOutPtrs& o, size_t smem, cudaStream_t stream);
-cudaError_t configure_ll_route(size_t smem);
+cudaError_t configure_ll_route(size_t needed, size_t optin);
 // Expert-major group offsets [E+1] from per-expert counts (one block).
 void launch_em_offsets(const int* count, int E, int align, int* offset, cudaStream_t stream);
 
@@ -215,6 +230,6 @@ struct LowLatencyOut {
 };
 void launch_ll_dispatch(const RouteParams& p, const LowLatencyOut& o, bool fp8, size_t smem,
                         cudaStream_t stream);
-cudaError_t configure_ll_dispatch(size_t smem);
+cudaError_t configure_ll_dispatch(size_t needed, size_t optin);
 
 }  // namespace ep

@@ -310,8 +310,8 @@ void launch_layout_tokens(const RouteParams& p, const LayoutOutPtrs& out, cudaSt
 
 size_t layout_tokens_smem(int R, int E, int CT, int kmax) { return layout_tokens_smem_bytes(R, E, CT, kmax); }
 
-cudaError_t configure_layout_tokens(size_t smem) {
-  return cudaFuncSetAttribute(k_layout_tokens, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+cudaError_t configure_layout_tokens(size_t needed, size_t optin) {
+  return set_dynamic_smem_limit(reinterpret_cast<const void*>(k_layout_tokens), needed, optin);
 }
 
 void launch_layout(const RouteParams& p, const LayoutOutPtrs& out, size_t smem, cudaStream_t stream) {
@@ -327,8 +327,8 @@ void launch_layout(const RouteParams& p, const LayoutOutPtrs& out, size_t smem, 
   (void)launch_kernel(k_layout, dim3(p.C), dim3(kRouteThreads), smem, stream, p, o);
 }
 
-cudaError_t configure_layout(size_t smem) {
-  return cudaFuncSetAttribute(k_layout, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+cudaError_t configure_layout(size_t needed, size_t optin, size_t* limit) {
+  return set_dynamic_smem_limit(reinterpret_cast<const void*>(k_layout), needed, optin, limit);
 }
 
 }  // namespace ep

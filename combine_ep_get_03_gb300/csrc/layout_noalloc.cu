@@ -23,14 +23,14 @@ static __device__ __align__(256) unsigned long long g_layout_scratch[kScratchWor
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 unsigned long long* g_scratch_ptr[kMaxDevices] = {};
-int g_smem_optin[kMaxDevices] = {};
+size_t g_smem_limit[kMaxDevices] = {};
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // Once per device, with that device current: the device address of the
-// scratch array (its host-side name is only a stand-in), the opt-in
-// shared-memory limit, and the layout kernel's limit set to it.
-ep_status_t device_setup(int dev, unsigned long long** scratch, int* smem_optin) {
+// scratch array (its host-side name is only a stand-in), and the layout
+// kernel's dynamic shared-memory limit (set from the opt-in maximum).
+ep_status_t device_setup(int dev, unsigned long long** scratch, size_t* smem_limit) {
   std::lock_guard<std::mutex> lock(g_setup_mutex);
   if (!g_scratch_ptr[dev]) {
     void* p = nullptr;
@@ -44,13 +44,14 @@ ep_status_t device_setup(int dev, unsigned long long** scratch, int* smem_optin)
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     // the layout kernel's shared-memory limit: the opt-in maximum, the value
     // handle creation also sets, so the two never lower it under each other
-    if (e == cudaSuccess) e = ep::configure_layout(static_cast<size_t>(optin));
+    size_t limit = 0;
+    if (e == cudaSuccess) e = ep::configure_layout(0, static_cast<size_t>(optin), &limit);
     if (e != cudaSuccess) return EP_ERR_CUDA;
     g_scratch_ptr[dev] = static_cast<unsigned long long*>(p);
-    g_smem_optin[dev] = optin;
+    g_smem_limit[dev] = limit;
   }
   *scratch = g_scratch_ptr[dev];
-  *smem_optin = g_smem_optin[dev];
+  *smem_limit = g_smem_limit[dev];
   return EP_OK;
 }
 
@@ -90,11 +91,11 @@ extern "C" ep_status_t ep_get_dispatch_layout_noalloc(int R, int E, int k, const
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return EP_ERR_CUDA;
   if (dev >= kMaxDevices) return EP_ERR_INVALID_ARG;
   unsigned long long* scratch = nullptr;
-  int optin = 0;
-  ep_status_t st = device_setup(dev, &scratch, &optin);
+  size_t smem_limit = 0;
+  ep_status_t st = device_setup(dev, &scratch, &smem_limit);
   if (st != EP_OK) return st;
   const size_t smem = ep::route_smem_bytes(NK, CT << lg, CT, kmax);
-  if (smem > static_cast<size_t>(optin)) return EP_ERR_INVALID_ARG;
+  if (smem > smem_limit) return EP_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
   if (T == 0) {

@@ -154,8 +154,8 @@ void launch_em_offsets(const int* count, int E, int align, int* offset, cudaStre
   (void)launch_kernel(k_em_offsets, dim3(1), dim3(kEmOffsetThreads), 0, stream, count, E, align, offset);
 }
 
-cudaError_t configure_ll_route(size_t smem) {
-  return cudaFuncSetAttribute(k_ll_route, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+cudaError_t configure_ll_route(size_t needed, size_t optin) {
+  return set_dynamic_smem_limit(reinterpret_cast<const void*>(k_ll_route), needed, optin);
 }
 
 void launch_ll_dispatch(const RouteParams& p, const LowLatencyOut& o, bool fp8, size_t smem,
@@ -166,12 +166,10 @@ void launch_ll_dispatch(const RouteParams& p, const LowLatencyOut& o, bool fp8, 
     (void)launch_kernel(k_ll_dispatch<false>, dim3(p.C), dim3(kRouteThreads), smem, stream, p, o);
 }
 
-cudaError_t configure_ll_dispatch(size_t smem) {
-  cudaError_t e = cudaFuncSetAttribute(k_ll_dispatch<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+cudaError_t configure_ll_dispatch(size_t needed, size_t optin) {
+  cudaError_t e = set_dynamic_smem_limit(reinterpret_cast<const void*>(k_ll_dispatch<true>), needed, optin);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_ll_dispatch<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(smem));
+  return set_dynamic_smem_limit(reinterpret_cast<const void*>(k_ll_dispatch<false>), needed, optin);
 }
 
 }  // namespace ep

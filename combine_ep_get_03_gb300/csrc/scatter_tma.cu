@@ -276,7 +276,7 @@ size_t scatter_smem_bytes(int H, int R, int E, bool fp8, int mode, int NS, int N
   return scatter_block_bytes(H, scatter_head_ints(mode, R, E), fp8, NS, NC);
 }
 
-cudaError_t configure_scatter(size_t smem_limit) {
+cudaError_t configure_scatter(size_t optin) {
   const void* ks[6] = {reinterpret_cast<const void*>(k_scatter<false, kSrcRanks>),
                        reinterpret_cast<const void*>(k_scatter<true, kSrcRanks>),
                        reinterpret_cast<const void*>(k_scatter<false, kSrcLowLatency>),
@@ -284,7 +284,7 @@ cudaError_t configure_scatter(size_t smem_limit) {
                        reinterpret_cast<const void*>(k_scatter<false, kSrcExpertMajor>),
                        reinterpret_cast<const void*>(k_scatter<true, kSrcExpertMajor>)};
   for (const void* k : ks) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_limit));
+    cudaError_t e = set_dynamic_smem_limit(k, 0, optin);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
