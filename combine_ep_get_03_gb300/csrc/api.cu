@@ -515,10 +515,10 @@ ep_status_t ep_layout_and_dispatch(ep_handle_t h, const void* topk_idx, int T, c
     return EP_ERR_INVALID_ARG;
   ep_status_t st = check_device(h);
   if (st != EP_OK) return st;
-  int fblocks = 0, fns = 0, fnc = 0;
+  int fblocks = 0, fns = 0, fnc = 0, fown = 0;
   if (static_cast<long long>(T) * h->kmax < (1LL << 31))
     ep::fused_config(ep::kSrcRanks, fp8, T, h->R, h->E, h->k, h->kmax, h->H, sms_for(h, num_sms), h->smem_optin,
-                     &fblocks, &fns, &fnc);
+                     &fblocks, &fns, &fnc, &fown);
   if (fblocks == 0) {
     // the general path: layout kernel, then the scatter
     if ((st = ep_get_dispatch_layout(h, topk_idx, T, nullptr, nullptr, nullptr, stream)) != EP_OK) return st;
@@ -527,6 +527,7 @@ ep_status_t ep_layout_and_dispatch(ep_handle_t h, const void* topk_idx, int T, c
   }
   ep::FusedArgs f = fused_args(h, topk_idx, static_cast<const uint16_t*>(x), topk_weights, T);
   f.redundant = static_cast<long long>(T) * h->k <= kFusedRedundantRankEntries ? 1 : 0;
+  f.own_first = fown;
   f.agg = h->fused_agg;
   f.dst = h->dst;
   f.idx32 = h->idx32;
@@ -613,13 +614,14 @@ ep_status_t ep_low_latency_dispatch(ep_handle_t h, const void* x, const void* to
     if (recv_count) return cuda_status(cudaMemsetAsync(recv_count, 0, sizeof(int) * h->E, s), "ll memset");
     return EP_OK;
   }
-  int fblocks = 0, fns = 0, fnc = 0;
+  int fblocks = 0, fns = 0, fnc = 0, own = 0;
   ep::fused_config(ep::kSrcLowLatency, fp8, T, h->R, h->E, h->k, h->kmax, h->H, sms_for(h, num_sms), h->smem_optin,
-                   &fblocks, &fns, &fnc);
+                   &fblocks, &fns, &fnc, &own);
   if (fblocks > 0) {
     // routing and row movement in one cooperative launch
     ep::FusedArgs f = fused_args(h, topk_idx, static_cast<const uint16_t*>(x), nullptr, T);
     f.M = M;
+    f.own_first = own;
     f.agg = h->fused_agg;
     f.ll_idx = h->ll_idx;
     f.ll_slot = h->ll_slot;
@@ -631,7 +633,8 @@ ep_status_t ep_low_latency_dispatch(ep_handle_t h, const void* x, const void* to
         EP_OK)
       return st;
     if (h->debug)
-      std::fprintf(stderr, "[ep] ll dispatch T=%d: fused, %d blocks, %d stages, %d consumers\n", T, fblocks, fns, fnc);
+      std::fprintf(stderr, "[ep] ll dispatch T=%d: fused, %d blocks, %d stages, %d consumers, %d own tokens first\n", T,
+                   fblocks, fns, fnc, own);
     h->T_ll = T;
     return EP_OK;
   }
@@ -799,12 +802,13 @@ ep_status_t ep_em_layout_and_dispatch(ep_handle_t h, const void* topk_idx, int T
     h->T_em = 0;
     return EP_OK;
   }
-  int fblocks = 0, fns = 0, fnc = 0;
+  int fblocks = 0, fns = 0, fnc = 0, fown = 0;
   ep::fused_config(ep::kSrcExpertMajor, fp8, T, h->R, h->E, h->k, h->kmax, h->H, sms_for(h, num_sms), h->smem_optin,
-                   &fblocks, &fns, &fnc);
+                   &fblocks, &fns, &fnc, &fown);
   if (fblocks > 0) {
     ep::FusedArgs f = fused_args(h, topk_idx, static_cast<const uint16_t*>(x), topk_weights, T);
     f.agg = h->fused_agg;
+    f.own_first = fown;
     f.ll_idx = h->em_idx;
     f.ll_slot = h->em_slot;
     f.recv_count = h->em_count;

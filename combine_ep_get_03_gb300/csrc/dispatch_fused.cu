@@ -15,12 +15,22 @@
 // Each block writes its counts (uint16), all blocks meet at one bounded grid
 // barrier (co-residency guaranteed by the cooperative launch), and each block
 // sums its predecessors' counts into exclusive prefixes.  Small batches skip
-// the barrier -- every block counts every entry itself -- in the per-entry
-// modes up to kFusedRedundantEntries entries, in the rank-major mode (its own
-// instantiation, kRedRanks, so that the large-batch code is untouched) up to
-// the host's smaller limit (tiny shape: 20.4 -> 16.2 us as graph replays).
+// the barrier and count the ids themselves: in the low-latency mode (up to
+// kFusedRedundantEntries entries) each block counts the entries of the tokens
+// before its own (16-byte id loads), and the block owning the last token
+// writes the per-expert totals; in the expert-major mode every block counts
+// every entry (each needs the totals for the group offsets); in the
+// rank-major mode (its own instantiation, kRedRanks, so that the large-batch
+// code is untouched, up to the host's smaller limit) every block counts every
+// token's ranks and experts (tiny shape: 20.4 -> 16.2 us as graph replays).
 // The block then writes its tokens' destinations and publishes them (a
 // per-block word set to the launch's generation + 1).
+//
+// Own rows.  A low-latency batch small enough for the counting above, whose
+// tokens per block fit a block's stage ring at once, moves each block's own
+// tokens instead of claiming (decode shape, 7 tokens per SM: each consumer
+// warp takes one token); the consumers then read their tokens' slots from
+// the block's shared-memory tables and wait for no other block.
 //
 // Rows.  The row movement is not tied to the routing's token runs: from the
 // first instruction on, the producer claims tokens two at a time from one
@@ -181,11 +191,71 @@ __device__ inline void column_sums_par(const uint16_t* agg, int ld, int ncols, i
   }
 }
 
+// Adds 1 to hist[e] for every id e in [0, E) among the first n ids of the
+// top-k table, with 16-byte loads where the table's alignment allows (the
+// ids are never written while the kernel runs).  Called by the consumer
+// threads (ct of nct).
+__device__ inline void count_ids_prefix(const void* ids, int ids32, long long n, int E, int* hist, int ct, int nct) {
+  auto add = [&](long long e) {
+    if (e >= 0 && e < E) atomicAdd(hist + e, 1);
+  };
+  const bool vec = (reinterpret_cast<uintptr_t>(ids) & 15) == 0;
+  if (vec && !ids32) {
+    const longlong2* v = static_cast<const longlong2*>(ids);
+    const long long nq = n >> 1;
+    for (long long q0 = ct; q0 < nq; q0 += 8LL * nct) {
+      longlong2 w[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const long long q = q0 + static_cast<long long>(j) * nct;
+        w[j] = q < nq ? __ldg(v + q) : make_longlong2(-1, -1);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        add(w[j].x);
+        add(w[j].y);
+      }
+    }
+    if ((n & 1) && ct == 0) add(static_cast<const long long*>(ids)[n - 1]);
+  } else if (vec) {
+    const int4* v = static_cast<const int4*>(ids);
+    const long long nq = n >> 2;
+    for (long long q0 = ct; q0 < nq; q0 += 8LL * nct) {
+      int4 w[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const long long q = q0 + static_cast<long long>(j) * nct;
+        w[j] = q < nq ? __ldg(v + q) : make_int4(-1, -1, -1, -1);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        add(w[j].x);
+        add(w[j].y);
+        add(w[j].z);
+        add(w[j].w);
+      }
+    }
+    for (long long i = (nq << 2) + ct; i < n; i += nct) add(static_cast<const int*>(ids)[i]);
+  } else {
+    for (long long i0 = ct; i0 < n; i0 += 16LL * nct) {
+      long long v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const long long i = i0 + static_cast<long long>(j) * nct;
+        v[j] = i < n ? load_topk_id(ids, i, ids32) : -1;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) add(v[j]);
+    }
+  }
+}
+
 // Routing tables in shared memory (int32 unless noted).
 __host__ __device__ inline size_t fused_route_bytes(int mode, int R, int E, int kmax, int kp, int tpb, int nc) {
   if (mode == kSrcRanks)
     return 8 * static_cast<size_t>(tpb)                        // token rank masks (u64)
            + 4 * static_cast<size_t>(tpb) * kmax               // local rows
+           + 8 * static_cast<size_t>(tpb) * kp                 // own tokens' ids and weights
            + 4 * (static_cast<size_t>(nc) * R + E + 3 * (R + 1) + 4);
   const size_t ni = static_cast<size_t>(tpb) * kp;
   const size_t em = 2 * static_cast<size_t>(E) + 1 + 32;  // totals, group offsets, scan scratch
@@ -245,17 +315,28 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
   const int tpb = fused_tokens_per_block(a.T, nb);
   const int t_begin = min(a.T, b * tpb);
   const int n_own = min(a.T, t_begin + tpb) - t_begin;
+  // phase-1 partition of the block's tokens (rank-major: one lane per token)
+  // and entries (per-entry modes) over the consumer warps, 32-aligned
+  const int tpw = ((tpb + NC - 1) / NC + 31) & ~31;
+  const int NI = tpb << a.kp_log2;
+  const int ipw = (((NI + NC - 1) / NC) + 31) & ~31;
 
   // ---- shared memory carve-up
   unsigned char* p = smem;
   unsigned long long* tmask = nullptr;
   int *tlocal = nullptr, *cnt = nullptr, *hist = nullptr, *so = nullptr, *excl = nullptr, *tot = nullptr;
   int *item_e = nullptr, *item_slot = nullptr, *etot = nullptr, *eoff = nullptr, *wsum = nullptr;
+  int* tids = nullptr;    // rank-major: the own tokens' ids [tpb][kp] (bad ids as -1)
+  float* tw = nullptr;    // and their top-k weights [tpb][kp] (when rows carry metadata)
   if (!kLL) {
     tmask = reinterpret_cast<unsigned long long*>(p);
     p += 8 * static_cast<size_t>(tpb);
     tlocal = reinterpret_cast<int*>(p);
     p += 4 * static_cast<size_t>(tpb) * kmax;
+    tids = reinterpret_cast<int*>(p);
+    p += 4 * static_cast<size_t>(tpb) * kp;
+    tw = reinterpret_cast<float*>(p);
+    p += 4 * static_cast<size_t>(tpb) * kp;
     cnt = reinterpret_cast<int*>(p);   // [NC][R]
     hist = cnt + NC * R;               // [E]
     so = hist + E;                     // [R+1] rank_offset
@@ -301,28 +382,39 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
     // its routing); when the claims run out it hands every consumer warp a
     // "no more" stage
     if (lane == 0) {
+      // first the block's own tokens [t_begin, t_begin + F0) -- all of them
+      // for small batches -- whose destinations its consumers read from
+      // shared memory; then claims of the rest: claim c names position
+      // F0 + c % rem of block c / rem (rem = tpb - F0 tokens per block),
+      // kClaimTokens at a time, one claim ahead
       unsigned* claim = a.barrier + kCtlClaim;
-      int base = static_cast<int>(atomicAdd(claim, static_cast<unsigned>(kClaimTokens)));
-      int next = base < a.T ? static_cast<int>(atomicAdd(claim, static_cast<unsigned>(kClaimTokens))) : a.T;
+      const int F0 = min(a.own_first, tpb);
+      const int rem = tpb - F0;
+      const int cmax = ((a.T + tpb - 1) / tpb) * rem;  // claims that can name a token
       int i = 0;
       bool ok = true;
-      while (ok && base < a.T) {
-        for (int c = 0; c < kClaimTokens && base + c < a.T; ++c, ++i) {
-          const int s = i % NS;
-          if (!kLL && i == kRouteStages && !mbar_wait(routed, 0u, a.err)) {
-            ok = false;
-            break;
+      auto put = [&](int t) -> bool {
+        const int s = i % NS;
+        if (!kLL && i == kRouteStages && !mbar_wait(routed, 0u, a.err)) return false;
+        if (i >= NS && !mbar_wait(empty + s, static_cast<uint32_t>((i / NS - 1) & 1), a.err)) return false;
+        stage_tok[s] = t;
+        mbar_arrive_expect_tx(full + s, row_bytes);
+        bulk_load(stage(s), a.x + static_cast<size_t>(t) * H, row_bytes, full + s);
+        ++i;
+        return true;
+      };
+      for (int tl = 0; ok && tl < min(F0, n_own); ++tl) ok = put(t_begin + tl);
+      if (ok && rem > 0) {
+        int base = static_cast<int>(atomicAdd(claim, static_cast<unsigned>(kClaimTokens)));
+        int next = base < cmax ? static_cast<int>(atomicAdd(claim, static_cast<unsigned>(kClaimTokens))) : cmax;
+        while (ok && base < cmax) {
+          for (int c = base; ok && c < base + kClaimTokens && c < cmax; ++c) {
+            const int t = (c / rem) * tpb + F0 + c % rem;
+            if (t < a.T) ok = put(t);
           }
-          if (i >= NS && !mbar_wait(empty + s, static_cast<uint32_t>((i / NS - 1) & 1), a.err)) {
-            ok = false;
-            break;
-          }
-          stage_tok[s] = base + c;
-          mbar_arrive_expect_tx(full + s, row_bytes);
-          bulk_load(stage(s), a.x + static_cast<size_t>(base + c) * H, row_bytes, full + s);
+          base = next;
+          if (base < cmax) next = static_cast<int>(atomicAdd(claim, static_cast<unsigned>(kClaimTokens)));
         }
-        base = next;
-        if (base < a.T) next = static_cast<int>(atomicAdd(claim, static_cast<unsigned>(kClaimTokens)));
       }
       for (int j = i; ok && j < i + NC; ++j) {
         const int s = j % NS;
@@ -336,11 +428,13 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
 
   const int cw = warp - 1;  // consumer warp
   const unsigned lt = lanemask_lt();
+  // rank-major rows carry source index / local ids / weights
+  const bool meta = !kLL && (a.recv_src_idx || a.recv_topk_idx || a.recv_topk_weights);
+  const bool w_own = meta && a.topk_weights;  // own tokens' weights kept in shared memory
   // ---------------------------------------------------------------- phase 1: rank the block's tokens
   if (!kLL) {
     for (int i = ct; i < E; i += nct) hist[i] = 0;
     consumer_sync(nct);
-    const int tpw = ((tpb + NC - 1) / NC + 31) & ~31;
     int run_lo = 0, run_hi = 0;
     for (int b0 = cw * tpw; b0 < min(n_own, (cw + 1) * tpw); b0 += 32) {  // warp-uniform
       const int tl = b0 + lane;
@@ -351,8 +445,12 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
         const long long ids = static_cast<long long>(t) * k;
         for (int j0 = 0; j0 < k; j0 += 8) {
           long long v[8];
+          float wv[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) v[j] = j0 + j < k ? load_topk_id(a.topk_idx, ids + j0 + j, a.ids32) : -1;
+          for (int j = 0; j < 8; ++j) {
+            v[j] = j0 + j < k ? load_topk_id(a.topk_idx, ids + j0 + j, a.ids32) : -1;
+            wv[j] = w_own && j0 + j < k ? a.topk_weights[ids + j0 + j] : 0.0f;
+          }
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             if (j0 + j >= k) break;
@@ -362,6 +460,8 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
               e = -1;
             }
             a.idx32[static_cast<size_t>(t) * k + j0 + j] = static_cast<int>(e);
+            tids[tl * kp + j0 + j] = static_cast<int>(e);
+            tw[tl * kp + j0 + j] = wv[j];
             if (e >= 0) {
               m |= 1ull << (static_cast<int>(e) / a.El);
               if (!kRedRanks) atomicAdd(hist + static_cast<int>(e), 1);
@@ -431,8 +531,6 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
       }
     }
   } else {
-    const int NI = tpb << a.kp_log2;
-    const int ipw = (((NI + NC - 1) / NC) + 31) & ~31;
     for (int i = ct; i < NC * E; i += nct) cnt[i] = 0;
     consumer_sync(nct);
     int* cntw = cnt + cw * E;
@@ -482,11 +580,20 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
         run += v;
       }
       if (!a.redundant) a.agg[static_cast<size_t>(b) * agg_ld(E) + col] = static_cast<uint16_t>(run);
+      else if (!kEM) etot[col] = run;  // the block's own entries per expert
     }
-    if (a.redundant) {
-      // small batches: every block counts every entry itself (entries of
-      // earlier tokens into excl, all of them into etot) instead of meeting
-      // the other blocks at the grid barrier
+    if (a.redundant && !kEM) {
+      // small batches, low latency: every block with tokens counts the
+      // entries of the tokens before its own (into excl) instead of meeting
+      // the other blocks at the grid barrier; the block owning the last token
+      // then has every expert's total (excl + its own entries)
+      for (int e = ct; e < E; e += nct) excl[e] = 0;
+      consumer_sync(nct);
+      if (n_own > 0) count_ids_prefix(a.topk_idx, a.ids32, static_cast<long long>(t_begin) * k, E, excl, ct, nct);
+    } else if (a.redundant) {
+      // small batches, expert-major: every block counts every entry itself
+      // (entries of earlier tokens into excl, all of them into etot: every
+      // block needs the totals for the group offsets)
       for (int e = ct; e < E; e += nct) excl[e] = etot[e] = 0;
       consumer_sync(nct);
       const long long n_all = static_cast<long long>(a.T) * k, n_before = static_cast<long long>(t_begin) * k;
@@ -546,22 +653,6 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
       }
     }
     consumer_sync(nct);
-    // each token's (rank, row-in-rank) list for the handle, and its global rows here
-    const int tpw = ((tpb + NC - 1) / NC + 31) & ~31;
-    for (int tl = ct; tl < n_own; tl += nct) {
-      const int t = t_begin + tl;
-      const int w = tl / tpw;
-      unsigned long long m = tmask[tl];
-      int pos = 0;
-      while (m) {
-        const int r = __ffsll(static_cast<long long>(m)) - 1;
-        m &= m - 1;
-        const int in_rank = excl[r] + cnt[w * R + r] + tlocal[tl * kmax + pos];
-        a.dst[static_cast<size_t>(t) * kmax + pos] = make_int2(r, in_rank);
-        ++pos;
-      }
-      for (; pos < kmax; ++pos) a.dst[static_cast<size_t>(t) * kmax + pos] = make_int2(-1, -1);
-    }
   } else {
     if (!a.redundant) {
       column_sums_par(a.agg, ld, E, nb, b, excl, kEM ? etot : nullptr, nct, ct);
@@ -582,49 +673,66 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
       if (ct == 0) eoff[E] = total;
       consumer_sync(nct);
     }
-    const int NI = tpb << a.kp_log2;
-    const int ipw = (((NI + NC - 1) / NC) + 31) & ~31;
-    for (int i = ct; i < n_own * kp; i += nct) {
-      const int tl = i >> a.kp_log2;
-      const int j = i & (kp - 1);
-      if (j >= k) continue;
-      const int t = t_begin + tl;
-      const int e = item_e[i];
-      int slot = -1;
-      if (e >= 0) {
-        slot = excl[e] + cnt[(i / ipw) * E + e] + item_slot[i];
-        if (!kEM && slot >= a.M) {
-          latch_error(a.err, kErrCapacity);
-          slot = -1;
+  }
+  consumer_sync(nct);  // the prefixes are final: every own token's destinations are known here
+  if (threadIdx.x == 32) mbar_arrive(routed);  // the producer may stream past kRouteStages rows (rank-major)
+
+  // The own tokens' destinations for the handle and for the other blocks'
+  // consumers: rank-major, each token's (rank, row-in-rank) list; per-entry
+  // modes, each entry's expert and slot.
+  auto write_own_destinations = [&]() {
+    if (!kLL) {
+      for (int tl = ct; tl < n_own; tl += nct) {
+        const int t = t_begin + tl;
+        const int w = tl / tpw;
+        unsigned long long m = tmask[tl];
+        int pos = 0;
+        while (m) {
+          const int r = __ffsll(static_cast<long long>(m)) - 1;
+          m &= m - 1;
+          const int in_rank = excl[r] + cnt[w * R + r] + tlocal[tl * kmax + pos];
+          a.dst[static_cast<size_t>(t) * kmax + pos] = make_int2(r, in_rank);
+          ++pos;
         }
+        for (; pos < kmax; ++pos) a.dst[static_cast<size_t>(t) * kmax + pos] = make_int2(-1, -1);
       }
-      a.ll_idx[static_cast<size_t>(t) * k + j] = e;
-      a.ll_slot[static_cast<size_t>(t) * k + j] = slot;
+    } else {
+      for (int i = ct; i < n_own * kp; i += nct) {
+        const int tl = i >> a.kp_log2;
+        const int j = i & (kp - 1);
+        if (j >= k) continue;
+        const int t = t_begin + tl;
+        const int e = item_e[i];
+        int slot = -1;
+        if (e >= 0) {
+          slot = excl[e] + cnt[(i / ipw) * E + e] + item_slot[i];
+          if (!kEM && slot >= a.M) {
+            latch_error(a.err, kErrCapacity);
+            slot = -1;
+          }
+        }
+        a.ll_idx[static_cast<size_t>(t) * k + j] = e;
+        a.ll_slot[static_cast<size_t>(t) * k + j] = slot;
+      }
     }
-  }
-  consumer_sync(nct);
-  if (threadIdx.x == 32) {  // this block's destinations are visible to every block
-    __threadfence();
-    st_release_u32(a.barrier + kCtlPub + b, gen + 1);
-    mbar_arrive(routed);  // the producer may stream past kRouteStages rows (rank-major)
-  }
+  };
 
   // ---------------------------------------------------------------- phase 3: move the rows
   unsigned char* qd = qbuf0 + static_cast<size_t>(cw) * (static_cast<size_t>(H) + ((4 * G + 15) & ~15));
   float* sd = reinterpret_cast<float*>(qd + H);
-  const bool meta = !kLL && (a.recv_src_idx || a.recv_topk_idx || a.recv_topk_weights);
   bool first = true;
   int owner_ok = b;  // the owning block whose destinations were last seen published
-  for (int i = cw;; i += NC) {
+  // ring item i (stage i % NS) of this consumer warp; false: no more items
+  auto step = [&](int i) -> bool {
     const int s = i % NS;
     const bool landed = mbar_wait(full + s, static_cast<uint32_t>((i / NS) & 1), a.err);
-    if (!__all_sync(kFullMask, landed)) break;
+    if (!__all_sync(kFullMask, landed)) return false;
     const int t = stage_tok[s];
     if (t >= a.T) latch_error(a.err, kErrState);  // never written by the producer: cannot happen
     if (t < 0 || t >= a.T) {  // no more rows
       __syncwarp();
       if (lane == 0) mbar_arrive(empty + s);
-      break;
+      return false;
     }
     // the owning block's destinations: published words, then plain L2 loads
     const int owner = t / tpb;
@@ -648,24 +756,53 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
     if (!have) {
       // gave up waiting (latched): the token's rows are skipped
     } else if (!kLL) {
-      if (lane < kmax) {
-        const int2 d = __ldcg(a.dst + static_cast<size_t>(t) * kmax + lane);
-        if (d.x >= 0) {
-          r = d.x;
-          row = static_cast<long long>(so[d.x]) + d.y;
-          if (row >= a.cap) {
-            latch_error(a.err, kErrCapacity);
-            row = -1;
+      if (owner == b) {
+        // the block's own token: destinations from its shared-memory tables
+        // (the values the routing phase published): the lane-th destination
+        // rank in ascending order, its row in the rank's region
+        const int tl = t - t_begin;
+        if (lane < kmax) {
+          unsigned long long m = tmask[tl];
+          for (int q = 0; q < lane && m; ++q) m &= m - 1;
+          if (m) {
+            r = __ffsll(static_cast<long long>(m)) - 1;
+            row = static_cast<long long>(so[r]) + excl[r] + cnt[(tl / tpw) * R + r] + tlocal[tl * kmax + lane];
           }
         }
+        if (meta && lane < k) {
+          e = tids[tl * kp + lane];
+          w = tw[tl * kp + lane];
+        }
+      } else {
+        if (lane < kmax) {
+          const int2 d = __ldcg(a.dst + static_cast<size_t>(t) * kmax + lane);
+          if (d.x >= 0) {
+            r = d.x;
+            row = static_cast<long long>(so[d.x]) + d.y;
+          }
+        }
+        if (meta && lane < k) {
+          e = __ldcg(a.idx32 + static_cast<size_t>(t) * k + lane);
+          if (a.topk_weights) w = a.topk_weights[static_cast<size_t>(t) * k + lane];
+        }
       }
-      if (meta && lane < k) {
-        e = __ldcg(a.idx32 + static_cast<size_t>(t) * k + lane);
-        if (a.topk_weights) w = a.topk_weights[static_cast<size_t>(t) * k + lane];
+      if (row >= a.cap) {
+        latch_error(a.err, kErrCapacity);
+        row = -1;
       }
     } else if (lane < k) {
-      const int ee = __ldcg(a.ll_idx + static_cast<size_t>(t) * k + lane);
-      const int sl = __ldcg(a.ll_slot + static_cast<size_t>(t) * k + lane);
+      int ee, sl;
+      if (owner == b) {
+        // the block's own token: its entries' experts and slots from shared
+        // memory (the values the routing phase published)
+        const int it = ((t - t_begin) << a.kp_log2) + lane;
+        ee = item_e[it];
+        sl = ee >= 0 ? excl[ee] + cnt[(it / ipw) * E + ee] + item_slot[it] : -1;
+        if (!kEM && sl >= a.M) sl = -1;  // over capacity (latched when published)
+      } else {
+        ee = __ldcg(a.ll_idx + static_cast<size_t>(t) * k + lane);
+        sl = __ldcg(a.ll_slot + static_cast<size_t>(t) * k + lane);
+      }
       if (ee >= 0 && sl >= 0) row = kEM ? static_cast<long long>(eoff[ee]) + sl : static_cast<long long>(ee) * a.M + sl;
       if (kEM && row >= a.cap) {
         latch_error(a.err, kErrCapacity);  // the row does not fit the receive buffer
@@ -731,6 +868,19 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
     } else if (kLL && a.recv_src_info && row >= 0) {
       st_keep(a.recv_src_info + row, t);
     }
+    return true;
+  };
+  // Publish this block's destinations (a consumer warp's first items are the
+  // block's own tokens, whose destinations it reads from shared memory; the
+  // other blocks need them for the tokens they claim), then move the rows in
+  // ring order.
+  write_own_destinations();
+  consumer_sync(nct);
+  if (threadIdx.x == 32) {  // this block's destinations are visible to every block
+    __threadfence();
+    st_release_u32(a.barrier + kCtlPub + b, gen + 1);
+  }
+  for (int i = cw; step(i); i += NC) {
   }
   if (kEM) {
     // padding rows of the groups this block owns (experts b, b + nb, ...):
@@ -750,12 +900,17 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
   }
   // per-expert totals (outputs only, nothing above waits for them): block b
   // forms the totals of experts e = b, b + nb, ...
-  for (int e = b + ct * nb; !kEM && e < E; e += nct * nb) {
-    const int all = kRedRanks ? hist[e] : kLL && a.redundant ? etot[e] : column_total(a.agg, ld, (kLL ? 0 : R) + e, nb);
-    if (kLL) {
-      if (a.recv_count) a.recv_count[e] = min(all, a.M);
-    } else {
-      a.recv_per_expert[e] = all;
+  if (kLL && !kEM && a.redundant) {
+    if (n_own > 0 && t_begin + n_own == a.T && a.recv_count)
+      for (int e = ct; e < E; e += nct) a.recv_count[e] = min(excl[e] + etot[e], a.M);
+  } else {
+    for (int e = b + ct * nb; !kEM && e < E; e += nct * nb) {
+      const int all = kRedRanks ? hist[e] : column_total(a.agg, ld, (kLL ? 0 : R) + e, nb);
+      if (kLL) {
+        if (a.recv_count) a.recv_count[e] = min(all, a.M);
+      } else {
+        a.recv_per_expert[e] = all;
+      }
     }
   }
   if (lane == 0) bulk_wait_all();
@@ -773,19 +928,30 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
   }
 }
 
-// Blocks, stages and consumers for the fused kernel; blocks = 0 when it does
-// not apply (R > 64 in normal mode, too many (token, k) entries per block,
-// rows too long for two stages).
+constexpr int kFusedMinStages = 8;
+
+// Blocks, stages and consumers for the fused kernel, and how many of its own
+// tokens each block streams before it claims others'; blocks = 0 when the
+// kernel does not apply (R > 64 in normal mode, too many (token, k) entries
+// per block, rows too long for two stages).  Each block first moves a full
+// ring of its own tokens (their destinations are in its shared memory as soon
+// as it has routed them).  A low-latency batch small enough for every block
+// to count the entries itself moves only each block's own tokens when they
+// fit its ring at once: then the most consumers whose ring still holds them
+// all (one token per consumer where possible).
 void fused_config(int mode, bool fp8, int T, int R, int E, int k, int kmax, int H, int sms, size_t smem_limit,
-                  int* blocks, int* NS, int* NC) {
+                  int* blocks, int* NS, int* NC, int* own_first) {
   *blocks = *NS = *NC = 0;
+  if (own_first) *own_first = 0;
   if (T <= 0 || (mode == kSrcRanks && R > 64)) return;
   int kp = 1;
   while (kp < k) kp <<= 1;
   const int nb = sms;
   const int tpb = fused_tokens_per_block(T, nb);
   if (tpb * kp > kFusedMaxItems) return;
+  const bool small = mode == kSrcLowLatency && static_cast<long long>(T) * k <= kFusedRedundantEntries;
   const int max_nc = fp8 ? kScatterMaxConsumers : 4;
+  int own_ns = 0, own_nc = 0;
   for (int pass = 0; pass < 2 && *NS == 0; ++pass) {
     // first at least half the consumers (the quantiser's compute), then any
     for (int nc = max_nc; nc >= (pass == 0 ? (max_nc + 1) / 2 : 1); --nc) {
@@ -795,13 +961,28 @@ void fused_config(int mode, bool fp8, int T, int R, int E, int k, int kmax, int 
       if (ns > 32) ns = 32;
       while (ns >= 2 && fused_smem_bytes(mode, fp8, R, E, kmax, kp, tpb, nc, ns, H) > smem_limit) --ns;
       ns -= ns % nc;  // consumer c owns the stages s = c (mod nc), as in k_scatter
-      if (ns >= 2 && ns >= nc && ns > *NS) {  // the most stages; more consumers on a tie
+      // the most consumers whose ring has at least kFusedMinStages stages (the
+      // quantiser's compute is spread over more warps: V3 shape, 8 consumers
+      // x 8 stages beat 6 x 12 by 1-3 us); failing that, the most stages
+      const bool enough = ns >= kFusedMinStages && *NS < kFusedMinStages;
+      if (ns >= 2 && ns >= nc && (enough || (*NS < kFusedMinStages && ns > *NS))) {
         *NS = ns;
         *NC = nc;
       }
+      if (small && own_ns == 0 && ns >= 2 && ns >= nc && ns >= tpb) {  // the most consumers that hold tpb
+        own_ns = ns;
+        own_nc = nc;
+      }
     }
   }
-  if (*NS > 0) *blocks = nb;
+  if (own_ns > 0) {
+    *NS = own_ns;
+    *NC = own_nc;
+  }
+  if (*NS > 0) {
+    *blocks = nb;
+    if (own_first) *own_first = own_ns > 0 ? tpb : (*NS < tpb ? *NS : tpb);
+  }
 }
 
 cudaError_t configure_fused(size_t optin) {

@@ -173,6 +173,7 @@ struct FusedArgs {
   const void* topk_idx;        // [T][k] int64, or int32 if ids32
   int ids32;
   int redundant;               // small batch: every block counts every entry, no grid barrier
+  int own_first;               // own tokens a block streams before claiming others' (>= tokens per block: no claims)
   const uint16_t* x;
   const float* topk_weights;
   int T, R, E, El, k, kp_log2, kmax, H, M;
@@ -207,7 +208,7 @@ struct FusedArgs {
   float* recv_scales;
 };
 void fused_config(int mode, bool fp8, int T, int R, int E, int k, int kmax, int H, int sms, size_t smem_limit,
-                  int* blocks, int* NS, int* NC);
+                  int* blocks, int* NS, int* NC, int* own_first);
 cudaError_t configure_fused(size_t optin);
 cudaError_t launch_fused(const FusedArgs& a, bool fp8, int mode, int blocks, int NS, int NC, cudaStream_t stream);
 

@@ -35,6 +35,8 @@ class EPError(RuntimeError):
 def lib() -> ctypes.CDLL:
     """Load the CUDA library (raises if it was not built)."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(LIB_PATH):
@@ -90,8 +92,15 @@ def _check(status: int, call: str) -> int:
     return status
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream) -> int:
     if stream is None:
+        # the current stream's handle without building a Stream object (a few
+        # microseconds a call, which the low-latency calls notice)
+        if _raw_stream is not None:
+            return _raw_stream(torch.cuda.current_device())
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, torch.cuda.Stream):
         return stream.cuda_stream

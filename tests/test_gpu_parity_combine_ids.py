@@ -30,7 +30,8 @@ def _inputs(R, E, k, H, tpr, seed, mask=0.02, dup=0.0):
     return idx, w, x
 
 
-CASES = [(4, 16, 2, 256, 16), (8, 64, 8, 1024, 64), (8, 256, 8, 7168, 96), (64, 256, 8, 512, 8), (3, 12, 4, 384, 33)]
+CASES = [(4, 16, 2, 256, 16), (8, 64, 8, 1024, 64), (8, 256, 8, 7168, 96), (64, 256, 8, 512, 8), (3, 12, 4, 384, 33),
+         (16, 64, 16, 1536, 12)]
 
 
 @pytest.mark.parametrize("case", CASES, ids=[f"R{c[0]}E{c[1]}k{c[2]}H{c[3]}t{c[4]}" for c in CASES])
@@ -55,6 +56,18 @@ def test_combine_fp8_input_and_weights(case):
         frac = assert_bf16_close(host_bits(out), ref_out, "e4m3 combine")
         assert frac == 1.0
         assert np.array_equal(cw.cpu().numpy().view(np.uint32), ref_cw.view(np.uint32)), "combined_topk_weights"
+        # without the weights' reduction (H a multiple of 512: the bulk-copy
+        # ring kernel), then with scales that are only 4-byte aligned (the
+        # register-resident kernel): the same values
+        out2 = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+        h.combine_ex(dev(q), out2, y_scales=dev(s))
+        assert np.array_equal(host_bits(out2), ref_out), "e4m3 combine without weights"
+        s_buf = torch.empty(s.size + 1, dtype=torch.float32, device=DEV)
+        s_off = s_buf[1:].view(P, H // 128)
+        s_off.copy_(dev(s))
+        out3 = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+        h.combine_ex(dev(q), out3, y_scales=s_off)
+        assert np.array_equal(host_bits(out3), ref_out), "e4m3 combine, 4-byte aligned scales"
     # bf16 y through the general entry point equals the plain combine
     y = wl.normal_bf16(g, (P, H))
     out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
@@ -207,5 +220,28 @@ def test_combine_ex_v3_workload():
     assert assert_bf16_close(host_bits(out), ref_out, "e4m3 combine, V3 shape") == 1.0
     assert np.array_equal(cw.cpu().numpy().view(np.uint32), ref_cw.view(np.uint32))
     assert np.array_equal(cw.cpu().numpy(), np.where(idx >= 0, wts, np.float32(0)))
+    # the same rows without the weights' reduction (the bulk-copy ring kernel)
+    out2 = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    h.combine_ex(recv, out2, y_scales=sc)
+    assert np.array_equal(host_bits(out2), ref_out)
+    assert h.get_device_status() == ep.EP_OK
+    h.close()
+
+
+def test_e4m3_combine_tokens_without_destinations():
+    """Tokens whose every entry is masked combine to +0 (the ring kernel's
+    items with no source), next to tokens with up to 16 sources."""
+    R, E, k, H, tpr = 16, 64, 16, 1024, 10
+    idx, w, x = _inputs(R, E, k, H, tpr, seed=91, mask=0.05)
+    idx[::3] = -1
+    h, L, ref, _ = normal_path(R, E, k, H, idx, w, x, fp8=True)
+    T = idx.shape[0]
+    out = torch.full((T, H), 7.0, dtype=torch.bfloat16, device=DEV)
+    P = int(L["rank_offset"][-1])
+    h.combine_ex(dev(ref["recv_x"][:P]), out, y_scales=dev(ref["recv_scales"][:P]))
+    ref_out, _ = oracle.combine_ex(R, E, k, idx, ref["recv_x"][:P], y_scales=ref["recv_scales"][:P])
+    got = host_bits(out)
+    assert np.array_equal(got, ref_out)
+    assert not got[::3].any()
     assert h.get_device_status() == ep.EP_OK
     h.close()
