@@ -356,7 +356,6 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
   uint64_t* empty = full + NS;
   uint64_t* routed = empty + NS;  // completes when this block has published its routing
   int* stage_tok = reinterpret_cast<int*>(routed + 2);  // token held by each stage (-1: no more)
-  unsigned* sh_gen = reinterpret_cast<unsigned*>(stage_tok + NS);
   unsigned char* stage0 = reinterpret_cast<unsigned char*>(stage_tok) + ((4 * NS + 4 + 15) & ~15);
   unsigned char* qbuf0 = stage0 + static_cast<size_t>(NS) * row_bytes;
   auto stage = [&](int s) { return stage0 + static_cast<size_t>(s) * row_bytes; };
@@ -368,12 +367,8 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
     }
     mbar_init(routed, 1);
     mbar_init_fence();
-    // the grid barrier's generation: written last by the previous launch (a
-    // relaxed load sees it), and it cannot change before this block arrives
-    *sh_gen = ld_relaxed_u32(a.barrier + 1);
   }
   __syncthreads();
-  const unsigned gen = *sh_gen;
 
   if (warp == 0) {
     // producer: claims tokens kClaimTokens at a time (one claim ahead) and
@@ -427,10 +422,17 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
   }
 
   const int cw = warp - 1;  // consumer warp
+  // the grid barrier's generation: written last by the previous launch (a
+  // relaxed load sees it), and it cannot change before this block has
+  // finished; read here, off the block's start-up path, and first used when
+  // the block publishes
+  const unsigned gen = ld_relaxed_u32(a.barrier + 1);
   const unsigned lt = lanemask_lt();
   // rank-major rows carry source index / local ids / weights
   const bool meta = !kLL && (a.recv_src_idx || a.recv_topk_idx || a.recv_topk_weights);
   const bool w_own = meta && a.topk_weights;  // own tokens' weights kept in shared memory
+  const bool vec8 = k == 8 && !a.ids32 && (reinterpret_cast<uintptr_t>(a.topk_idx) & 15) == 0 &&
+                    (!w_own || (reinterpret_cast<uintptr_t>(a.topk_weights) & 15) == 0);
   // ---------------------------------------------------------------- phase 1: rank the block's tokens
   if (!kLL) {
     for (int i = ct; i < E; i += nct) hist[i] = 0;
@@ -446,10 +448,29 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
         for (int j0 = 0; j0 < k; j0 += 8) {
           long long v[8];
           float wv[8];
+          if (vec8) {
+            const longlong2* p2 = reinterpret_cast<const longlong2*>(static_cast<const long long*>(a.topk_idx) + ids);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            v[j] = j0 + j < k ? load_topk_id(a.topk_idx, ids + j0 + j, a.ids32) : -1;
-            wv[j] = w_own && j0 + j < k ? a.topk_weights[ids + j0 + j] : 0.0f;
+            for (int j = 0; j < 4; ++j) {
+              const longlong2 q = __ldg(p2 + j);
+              v[2 * j] = q.x;
+              v[2 * j + 1] = q.y;
+            }
+            if (w_own) {
+              const float4* w4 = reinterpret_cast<const float4*>(a.topk_weights + ids);
+              const float4 w0 = __ldg(w4), w1 = __ldg(w4 + 1);
+              wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w;
+              wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) wv[j] = 0.0f;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              v[j] = j0 + j < k ? load_topk_id(a.topk_idx, ids + j0 + j, a.ids32) : -1;
+              wv[j] = w_own && j0 + j < k ? a.topk_weights[ids + j0 + j] : 0.0f;
+            }
           }
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
