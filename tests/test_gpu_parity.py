@@ -182,6 +182,20 @@ def test_fused_on_few_sms(num_sms):
     h.close()
 
 
+@pytest.mark.parametrize("num_sms", [16, 15, 152])
+def test_ll_own_rows_boundary(num_sms):
+    """Small low-latency batches move each block's own tokens when they fit
+    its ring (16 SMs: exactly 8 tokens per block, one per consumer warp) and
+    claim tokens otherwise (15 SMs: 9 per block); every block counts the ids
+    of the tokens before its own. The same results either way."""
+    R, E, k, H, tpr = 8, 64, 8, 1024, 16
+    idx, w, x = _edge_inputs(R, E, k, H, tpr, 0.03, 0.1, seed=80 + num_sms)
+    h = ep.Handle(R, E, k, H, tpr)
+    for fp8 in (True, False):
+        ll_path(R, E, k, H, idx, w, x, fp8=fp8, y_seed=81, handle=h, num_sms=num_sms)
+    h.close()
+
+
 @pytest.mark.parametrize("case", [(128, 128, 4, 128, 2), (8, 64, 8, 128, 10240)],
                          ids=["R128_layout_kernel", "T81920_routing_kernels"])
 def test_fused_falls_back_to_separate_kernels(case):
