@@ -26,26 +26,28 @@
 // The block then writes its tokens' destinations and publishes them (a
 // per-block word set to the launch's generation + 1).
 //
-// Own rows.  A low-latency batch small enough for the counting above, whose
-// tokens per block fit a block's stage ring at once, moves each block's own
-// tokens instead of claiming (decode shape, 7 tokens per SM: each consumer
-// warp takes one token); the consumers then read their tokens' slots from
-// the block's shared-memory tables and wait for no other block.
+// Rows.  The row movement is not tied to the routing's token runs.  Each
+// block first streams a full ring of its own tokens (the first NS of its
+// run): their destinations are in its shared-memory tables as soon as its
+// prefixes are final, so its consumers start on them without waiting for any
+// other block or reading anything back from L2.  Then the producer claims
+// the remaining tokens two at a time from one global counter (claim c names
+// position F0 + c mod (tpb - F0) of block c / (tpb - F0), F0 the tokens each
+// block moves first), one claim ahead, so that an SM that moves rows faster
+// takes more of them (the SMs of one GB300 do not all stream at the same
+// rate); a consumer reads a claimed token's destinations from global memory
+// once the owning block has published them.  In the rank-major mode the
+// producer streams only the first kRouteStages rows before the block's
+// prefixes are final: a full ring of row loads from every SM queues ahead of
+// the routing's dependent loads and delays it.  The per-entry modes keep the
+// full ring (their consumers start with eight stores a row).  Consumers
+// quantise / store a row exactly as k_scatter does.  Per-expert totals, which
+// nothing waits for, are formed after the rows.
 //
-// Rows.  The row movement is not tied to the routing's token runs: from the
-// first instruction on, the producer claims tokens two at a time from one
-// global counter and streams their rows into the shared-memory stage ring (the
-// rows do not depend on the routing), so an SM that moves rows faster takes
-// more of them (the SMs of one GB300 do not all stream at the same rate).  In
-// the rank-major mode it streams only the first kRouteStages rows before its
-// own block has published the routing: a full ring of row loads from every SM
-// queues ahead of the routing's dependent loads and delays it (V3 shape:
-// 88.3 -> 86.4 us).  The per-entry modes keep the full ring (their consumers
-// start with eight stores a row, and the cap cost them 1-2 us).  A
-// consumer reads a claimed token's destinations from global memory once the
-// owning block has published them, then quantises / stores the row exactly as
-// k_scatter does.  Per-expert totals, which nothing waits for, are formed
-// after the rows.
+// Own rows.  A low-latency batch small enough for the counting above, whose
+// tokens per block fit a block's stage ring at once, moves only each block's
+// own tokens (decode shape, 7 tokens per SM: each consumer warp takes one
+// token), with no claims at all.
 //
 // Rows and slots come out identical to the separate routing kernels: (source
 // rank, token) order per rank, (source rank, token, k) order per expert.  The
@@ -371,11 +373,10 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
   __syncthreads();
 
   if (warp == 0) {
-    // producer: claims tokens kClaimTokens at a time (one claim ahead) and
-    // streams their rows into the stages (rank-major: the first kRouteStages
-    // from the first instruction on, the rest once this block has published
-    // its routing); when the claims run out it hands every consumer warp a
-    // "no more" stage
+    // producer: streams rows into the stages (rank-major: the first
+    // kRouteStages from the first instruction on, the rest once this block's
+    // prefixes are final); when the tokens run out it hands every consumer
+    // warp a "no more" stage
     if (lane == 0) {
       // first the block's own tokens [t_begin, t_begin + F0) -- all of them
       // for small batches -- whose destinations its consumers read from

@@ -120,8 +120,8 @@ const void* combine_kernel(int src, bool fp8);
 constexpr int kCtlClaim = 2, kCtlDone = 3, kCtlPub = 4;
 constexpr int kClaimTokens = 2;  // tokens per claim
 // Rows a fused-kernel producer streams in, in the rank-major mode, before its
-// own block has published its routing: more would queue ahead of the
-// routing's dependent loads.
+// own block's prefixes are final: more would queue ahead of the routing's
+// dependent loads.
 constexpr int kRouteStages = 2;
 
 // TMA bulk-copy scatter (dispatch row movement), persistent: one block per
