@@ -70,6 +70,9 @@ __device__ __forceinline__ void add_scaled2(float& a0, float& a1, float p0, floa
   a1 = __fadd_rn(a1, __fmul_rn(p1, s));
 }
 
+// Asks L2 for the line holding p; nothing waits for it.
+__device__ __forceinline__ void pf_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" : : "l"(p)); }
+
 template <int kSrc, bool kFP8>
 __global__ void __launch_bounds__(kCombineThreads, kFP8 ? 3 : 2) k_combine(CombineArgs a) {
   extern __shared__ int base_smem[];  // rank_offset [R+1] or expert_offset [E+1]
@@ -183,6 +186,21 @@ __global__ void __launch_bounds__(kCombineThreads, kFP8 ? 3 : 2) k_combine(Combi
               } else {
                 const uint16_t* yb = static_cast<const uint16_t*>(a.y);
                 v[s][c] = ch < h_end ? ld_stream(yb + r_ * a.H + ch) : make_uint4(0, 0, 0, 0);
+              }
+            }
+          }
+        }
+        if (kFP8) {
+          // e4m3 sources come two at a time (register budget): ask L2 for the
+          // next two while these are summed (90.1 vs 92.2 us on the V3 shape)
+#pragma unroll
+          for (int s = 0; s < kBatch; ++s) {
+            const long long r_ = __shfl_sync(kFullMask, srow, (sb + kBatch + s) & 31);
+            if (sb + kBatch + s < n) {
+#pragma unroll
+              for (int c = 0; c < kChunks; ++c) {
+                const int ch = h0 + (c * 32 + lane) * kLaneCh;
+                if (ch < h_end) pf_l2(static_cast<const uint8_t*>(a.y) + r_ * a.H + ch);
               }
             }
           }
