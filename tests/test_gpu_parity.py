@@ -182,6 +182,24 @@ def test_fused_on_few_sms(num_sms):
     h.close()
 
 
+@pytest.mark.parametrize("num_sms", [152, 64, 24])
+def test_fused_own_tokens_first_with_claims(num_sms):
+    """Rank-major batches past the small-batch limit (the grid barrier):
+    every block moves a ring of its own tokens first (destinations from its
+    shared memory), then claims the rest -- none left at 7 tokens per block
+    (152 SMs), 8 of 16 (64 SMs), 35 of 43 (24 SMs). Rows, metadata and the
+    combine of them against the oracle; then the low-latency dispatch on the
+    same handle (the per-entry routing with the same rows order)."""
+    R, E, k, H, tpr = 8, 256, 8, 1024, 128
+    idx, w, x = _edge_inputs(R, E, k, H, tpr, 0.02, 0.05, seed=90 + num_sms)
+    y = wl.normal_bf16(wl.rng(91), (int(oracle.layout(R, E, k, idx)["rank_offset"][-1]), H))
+    h = ep.Handle(R, E, k, H, tpr)
+    for fp8 in (True, False):
+        fused_path(R, E, k, H, idx, w, x, fp8=fp8, y=y, handle=h, num_sms=num_sms)
+    ll_path(R, E, k, H, idx, w, x, fp8=True, y_seed=92, handle=h, num_sms=num_sms)
+    h.close()
+
+
 @pytest.mark.parametrize("num_sms", [16, 15, 152])
 def test_ll_own_rows_boundary(num_sms):
     """Small low-latency batches move each block's own tokens when they fit
