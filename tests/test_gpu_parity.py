@@ -427,3 +427,48 @@ def test_ll_path_captures_in_a_cuda_graph():
     assert torch.equal(out_graph.view(torch.int16), out_eager.view(torch.int16))
     assert h.get_device_status() == ep.EP_OK
     h.close()
+
+
+@pytest.mark.parametrize("num_sms", [0, 3])
+def test_ll_capacity_overflow_and_bad_id_latched(num_sms):
+    """Low-latency dispatch on a small batch (own rows on every SM, claims on
+    3 SMs): one expert receives more entries than its M rows (duplicated
+    ids), and one id is out of range. Both conditions are latched; the first
+    M entries of the full expert land where the oracle puts them, the bad id
+    counts as masked, and the combine of the dispatched rows matches the
+    oracle's, which skips the entries that got no row."""
+    R, E, k, H, tpr = 4, 16, 4, 256, 16
+    T = R * tpr
+    g = wl.rng(97 + num_sms)
+    idx, w = wl.route_uniform(g, T, E, k)
+    idx[:, :] = np.where(np.arange(T)[:, None] % 2 == 0, 5, idx)  # even tokens: all four entries on expert 5
+    idx[3, 2] = E + 3
+    x = wl.normal_bf16(g, (T, H))
+    h = ep.Handle(R, E, k, H, tpr)
+    M = h.M
+    recv = torch.zeros((E, M, H), dtype=torch.uint8, device=DEV)
+    scales = torch.zeros((E, M, H // 128), dtype=torch.float32, device=DEV)
+    src = torch.full((E, M), -7, dtype=torch.int32, device=DEV)
+    cnt = torch.full((E,), -7, dtype=torch.int32, device=DEV)
+    h.low_latency_dispatch(dev(x), dev(idx), ep.EP_FP8_E4M3, recv, scales, recv_src_info=src, recv_count=cnt,
+                           num_sms=num_sms)
+    st = h.get_device_status()
+    assert st in (ep.EP_ERR_BAD_EXPERT, ep.EP_ERR_CAPACITY)  # the first condition wins the latch
+    fixed = idx.copy()
+    fixed[3, 2] = -1
+    ref, rst = oracle.ll_dispatch(R, E, k, M, x, fixed, fp8=True)
+    assert rst == oracle.CAPACITY
+    count = cnt.cpu().numpy()
+    assert np.array_equal(count, ref["recv_count"])
+    assert count[5] == M
+    flat = np.concatenate([e * M + np.arange(c) for e, c in enumerate(count)]).astype(np.int64)
+    fl = torch.from_numpy(flat).to(DEV)
+    assert np.array_equal(recv.view(E * M, H)[fl].cpu().numpy(), ref["recv_x"].reshape(E * M, H)[flat])
+    assert np.array_equal(src.view(-1)[fl].cpu().numpy(), ref["recv_src_info"].reshape(-1)[flat])
+    y_host = np.zeros((E, M, H), np.uint16)
+    y_host.reshape(E * M, H)[flat] = wl.normal_bf16(wl.rng(98), (flat.size, H))
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    h.low_latency_combine(dev(y_host), dev(w), out, num_sms=num_sms)
+    assert np.array_equal(host_bits(out), oracle.ll_combine(R, E, k, M, fixed, w, y_host))
+    assert h.get_device_status() == ep.EP_OK
+    h.close()
