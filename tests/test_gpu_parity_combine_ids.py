@@ -56,9 +56,8 @@ def test_combine_fp8_input_and_weights(case):
         frac = assert_bf16_close(host_bits(out), ref_out, "e4m3 combine")
         assert frac == 1.0
         assert np.array_equal(cw.cpu().numpy().view(np.uint32), ref_cw.view(np.uint32)), "combined_topk_weights"
-        # without the weights' reduction (H a multiple of 512: the bulk-copy
-        # ring kernel), then with scales that are only 4-byte aligned (the
-        # register-resident kernel): the same values
+        # without the weights' reduction, then with scales that are only
+        # 4-byte aligned: the same values
         out2 = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
         h.combine_ex(dev(q), out2, y_scales=dev(s))
         assert np.array_equal(host_bits(out2), ref_out), "e4m3 combine without weights"
@@ -220,7 +219,7 @@ def test_combine_ex_v3_workload():
     assert assert_bf16_close(host_bits(out), ref_out, "e4m3 combine, V3 shape") == 1.0
     assert np.array_equal(cw.cpu().numpy().view(np.uint32), ref_cw.view(np.uint32))
     assert np.array_equal(cw.cpu().numpy(), np.where(idx >= 0, wts, np.float32(0)))
-    # the same rows without the weights' reduction (the bulk-copy ring kernel)
+    # the same rows without the weights' reduction
     out2 = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
     h.combine_ex(recv, out2, y_scales=sc)
     assert np.array_equal(host_bits(out2), ref_out)
@@ -229,8 +228,9 @@ def test_combine_ex_v3_workload():
 
 
 def test_e4m3_combine_tokens_without_destinations():
-    """Tokens whose every entry is masked combine to +0 (the ring kernel's
-    items with no source), next to tokens with up to 16 sources."""
+    """Tokens whose every entry is masked combine to +0 (no source enters the
+    three-slab register ring), next to tokens with up to 16 sources (the ring
+    wraps five times)."""
     R, E, k, H, tpr = 16, 64, 16, 1024, 10
     idx, w, x = _inputs(R, E, k, H, tpr, seed=91, mask=0.05)
     idx[::3] = -1
