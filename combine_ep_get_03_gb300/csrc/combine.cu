@@ -126,11 +126,16 @@ __global__ void __launch_bounds__(kCombineThreads, kFP8 ? 3 : 2) k_combine(Combi
     for (int e = threadIdx.x; e <= a.E; e += kCombineThreads) base_smem[e] = a.expert_offset[e];
     __syncthreads();
   }
+  // a warp's sources, compacted into summation order
+  __shared__ long long s_row[kCombineWarps][32];
+  __shared__ float s_w[kCombineWarps][32];
+  // item i = (token i / parts, part i % parts); warp w takes items w, w + nw,
+  // ..., stepping (token, part) by (dq, dr) with a carry instead of dividing
   const int parts = (a.H + kPartChannels - 1) / kPartChannels;
-  const long long items = static_cast<long long>(a.T) * parts;
-  for (long long item = blockIdx.x * kCombineWarps + warp; item < items; item += nw) {
-    const int t = static_cast<int>(item / parts);
-    const int part = static_cast<int>(item - static_cast<long long>(t) * parts);
+  const int first = blockIdx.x * kCombineWarps + warp;
+  const int dq = nw / parts, dr = nw - dq * parts;
+  int t = first / parts, part = first - t * parts;
+  for (; t < a.T;) {
     long long row = -1;
     float w = 0.0f;
     int key = INT_MAX;
@@ -167,14 +172,16 @@ __global__ void __launch_bounds__(kCombineThreads, kFP8 ? 3 : 2) k_combine(Combi
         pos += (kj < key || (kj == key && jj < lane)) ? 1 : 0;
       }
     }
-    // lane s receives the s-th source's row (and weight)
-    int from = 0;
-    for (int s = 0; s < n; ++s) {
-      const unsigned b = __ballot_sync(kFullMask, valid && pos == s);
-      if (lane == s) from = __ffs(b) - 1;
+    // lane s receives the s-th source's row (and weight); the valid lanes'
+    // positions are distinct, so each slot below n is written once
+    if (valid) {
+      s_row[warp][pos] = row;
+      if (kSrc == kSrcLowLatency) s_w[warp][pos] = w;
     }
-    const long long srow = __shfl_sync(kFullMask, row, from);
-    const float sw = __shfl_sync(kFullMask, w, from);
+    __syncwarp();
+    const long long srow = lane < n ? s_row[warp][lane] : -1;
+    const float sw = kSrc == kSrcLowLatency && lane < n ? s_w[warp][lane] : 0.0f;
+    __syncwarp();  // read before the next item writes
 
     if (kSrc == kSrcRanks && a.recv_topk_weights && part == 0) {
       // the top-k weights, column `lane`, summed over the same rows in order
@@ -271,6 +278,12 @@ __global__ void __launch_bounds__(kCombineThreads, kFP8 ? 3 : 2) k_combine(Combi
           }
         }
       }
+    }
+    part += dr;
+    t += dq;
+    if (part >= parts) {
+      part -= parts;
+      ++t;
     }
   }
 }
