@@ -65,7 +65,7 @@ KERNEL_SOURCES = {"k_combine<normal>": ["combine.cu", "device_common.cuh", "ep_i
 # ncu capture of the V3-shaped workload, keyed by the kernel's source digest:
 # a kernel whose sources changed since its capture reports traffic = null.
 MEASURED_TRAFFIC = {"k_combine<normal>": ("b4ecbbda27ba1fe6", 693837056),
-                    "k_route_scatter<fp8>": ("a2c42440633a2814", 382554624)}
+                    "k_route_scatter<fp8>": ("0ab9da6adae334cd", 382506240)}
 
 
 def kernel_digest(kernel: str) -> str:
@@ -593,25 +593,30 @@ def ll_decode_latency(dev: torch.device, reps: int = 200):
         torch.cuda.synchronize(dev)
         ts = sorted(ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(reps))
         res[name + "_us"] = round(ts[len(ts) // 2], 2)
-    # the pair as graph replays (launch overhead amortised)
-    s = torch.cuda.Stream(dev)
-    s.wait_stream(torch.cuda.current_stream(dev))
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(s):
-        with torch.cuda.graph(g, stream=s):
-            for _ in range(10):
-                disp()
-                comb()
-    torch.cuda.current_stream(dev).wait_stream(s)
-    g.replay()
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(20):
+    # each call alone and the pair as graph replays (launch overhead amortised)
+    def graph_us(calls):
+        s = torch.cuda.Stream(dev)
+        s.wait_stream(torch.cuda.current_stream(dev))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(10):
+                    for fn in calls:
+                        fn()
+        torch.cuda.current_stream(dev).wait_stream(s)
         g.replay()
-    e1.record()
-    torch.cuda.synchronize(dev)
-    pair_us = e0.elapsed_time(e1) * 1e3 / 200
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(20):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) * 1e3 / 200
+
+    res["dispatch_graph_us"] = round(graph_us([disp]), 2)
+    res["combine_graph_us"] = round(graph_us([comb]), 2)
+    pair_us = graph_us([disp, comb])
     n_ll = int(cnt.sum().item())
     res["pair_graph_us"] = round(pair_us, 2)
     res["logical_gbs_graph"] = round(n_ll * (w.H + 4 * G + 2 * w.H) / (pair_us / 1e6) / 1e9, 1)

@@ -432,7 +432,7 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
   // rank-major rows carry source index / local ids / weights
   const bool meta = !kLL && (a.recv_src_idx || a.recv_topk_idx || a.recv_topk_weights);
   const bool w_own = meta && a.topk_weights;  // own tokens' weights kept in shared memory
-  const bool vec8 = k == 8 && !a.ids32 && (reinterpret_cast<uintptr_t>(a.topk_idx) & 15) == 0 &&
+  const bool vec8 = k == 8 && (reinterpret_cast<uintptr_t>(a.topk_idx) & 15) == 0 &&
                     (!w_own || (reinterpret_cast<uintptr_t>(a.topk_weights) & 15) == 0);
   // ---------------------------------------------------------------- phase 1: rank the block's tokens
   if (!kLL) {
@@ -450,12 +450,19 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
           long long v[8];
           float wv[8];
           if (vec8) {
-            const longlong2* p2 = reinterpret_cast<const longlong2*>(static_cast<const long long*>(a.topk_idx) + ids);
+            if (a.ids32) {  // a token's eight int32 ids: two 16-byte loads
+              const int4* p4 = reinterpret_cast<const int4*>(static_cast<const int*>(a.topk_idx) + ids);
+              const int4 q0 = __ldg(p4), q1 = __ldg(p4 + 1);
+              v[0] = q0.x; v[1] = q0.y; v[2] = q0.z; v[3] = q0.w;
+              v[4] = q1.x; v[5] = q1.y; v[6] = q1.z; v[7] = q1.w;
+            } else {
+              const longlong2* p2 = reinterpret_cast<const longlong2*>(static_cast<const long long*>(a.topk_idx) + ids);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const longlong2 q = __ldg(p2 + j);
-              v[2 * j] = q.x;
-              v[2 * j + 1] = q.y;
+              for (int j = 0; j < 4; ++j) {
+                const longlong2 q = __ldg(p2 + j);
+                v[2 * j] = q.x;
+                v[2 * j + 1] = q.y;
+              }
             }
             if (w_own) {
               const float4* w4 = reinterpret_cast<const float4*>(a.topk_weights + ids);

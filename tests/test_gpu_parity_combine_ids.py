@@ -165,6 +165,59 @@ def test_int32_ids_every_routing_path(case):
     h.close()
 
 
+def test_int32_ids_fused_v3_workload():
+    """Full V3 shape with int32 ids through the fused layout + FP8 dispatch
+    (a token's eight ids read as two 16-byte words): every output equals the
+    oracle's, which routes the same ids as int64."""
+    w_ = wl.WORKLOADS["v3_ep8"]
+    x, idx, wts = wl.make_inputs(w_)
+    R, E, k, H = w_.R, w_.E, w_.k, w_.H
+    h = _handle32(R, E, k, H, w_.tokens_per_rank)
+    ref, _ = oracle.dispatch(R, E, k, x, idx, wts, fp8=True)
+    L = oracle.layout(R, E, k, idx)
+    P = int(L["rank_offset"][-1])
+    recv = torch.empty((P, H), dtype=torch.uint8, device=DEV)
+    sc = torch.empty((P, H // 128), dtype=torch.float32, device=DEV)
+    src = torch.full((P,), -7, dtype=torch.int32, device=DEV)
+    ridx = torch.full((P, k), -7, dtype=torch.int32, device=DEV)
+    rw = torch.full((P, k), -7.0, dtype=torch.float32, device=DEV)
+    h.layout_and_dispatch(dev(idx.astype(np.int32)), dev(x), dev(wts), ep.EP_FP8_E4M3, recv, sc, recv_src_idx=src,
+                          recv_topk_idx=ridx, recv_topk_weights=rw)
+    _, _, offset, _ = h.get_num_recv()
+    assert np.array_equal(offset, L["rank_offset"])
+    assert np.array_equal(recv.cpu().numpy(), ref["recv_x"][:P])
+    assert np.array_equal(sc.cpu().numpy().view(np.uint32), ref["recv_scales"][:P].view(np.uint32))
+    assert np.array_equal(src.cpu().numpy(), ref["recv_src_idx"][:P])
+    assert np.array_equal(ridx.cpu().numpy(), ref["recv_topk_idx"][:P])
+    assert np.array_equal(rw.cpu().numpy().view(np.uint32), ref["recv_topk_weights"][:P].view(np.uint32))
+    assert h.get_device_status() == ep.EP_OK
+    h.close()
+
+
+def test_int32_ids_fused_k8_bad_id_latched():
+    """An out-of-range int32 id among a token's eight (the 16-byte id loads)
+    is latched and routed nowhere; the other ids route as the oracle does
+    with that entry masked."""
+    R, E, k, H, tpr = 8, 64, 8, 256, 16
+    idx, w, x = _inputs(R, E, k, H, tpr, seed=23)
+    bad = idx.astype(np.int32)
+    bad[5, 3] = E
+    h = _handle32(R, E, k, H, tpr)
+    masked = idx.copy()
+    masked[5, 3] = -1
+    L = oracle.layout(R, E, k, masked)
+    P = int(L["rank_offset"][-1])
+    recv = torch.empty((max(P, 1), H), dtype=torch.uint8, device=DEV)[:P]
+    sc = torch.empty((max(P, 1), H // 128), dtype=torch.float32, device=DEV)[:P]
+    h.layout_and_dispatch(dev(bad), dev(x), dev(w), ep.EP_FP8_E4M3, recv, sc)
+    assert h.get_device_status() == ep.EP_ERR_BAD_EXPERT
+    _, _, offset, _ = h.get_num_recv()
+    assert np.array_equal(offset, L["rank_offset"])
+    ref, _ = oracle.dispatch(R, E, k, x, masked, w, fp8=True)
+    assert np.array_equal(recv.cpu().numpy(), ref["recv_x"][:P])
+    h.close()
+
+
 def test_int32_ids_bad_id_latched_and_width_checked():
     R, E, k, H, tpr = 4, 16, 2, 128, 8
     idx, w, x = _inputs(R, E, k, H, tpr, seed=17)
