@@ -9,7 +9,7 @@
 // loads in flight through a ring of stages, and NC consumer warps quantise
 // and store, so both the bytes in flight and the quantisation warps are
 // bounded by shared memory rather than registers.  The producer claims
-// tokens two at a time from one global counter, so SMs that move rows
+// tokens one at a time from one global counter, so SMs that move rows
 // faster take more of them (the SMs of one GB300 do not stream at one rate).
 //
 // Destinations:  normal  -- the handle's (rank, row-in-rank) list + the
