@@ -248,20 +248,24 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_scatter(
 }
 
 // Consumers and stages for a block: FP8 wants compute warps (8 consumers, the
-// rest of shared memory as stages); BF16 only moves bytes (4 consumers, more
-// stages).  NS is a multiple of NC.  Fewer consumers if the rows are long; 0
-// if not even two stages fit.
+// rest of shared memory as stages); BF16 only moves bytes: 2 consumers over
+// at most 4 stages (V3-shaped BF16 dispatch 115.1 us, against 118.3 with 4
+// consumers over all the stages that fit, 116.3 with 4 x 8, 116.5 with
+// 3 x 3, 125-133 with 1 x 2, 1 x 4 or 2 x 2: fewer rows in flight per SM
+// queue less in front of the HBM).  NS is a multiple of NC.  Fewer consumers
+// if the rows are long; 0 if not even two stages fit.
 void scatter_config(int H, int R, int E, bool fp8, int mode, size_t smem_limit, int* NS, int* NC) {
   *NS = 0;
   *NC = 0;
-  const int max_nc = fp8 ? kScatterMaxConsumers : 4;
+  const int max_nc = fp8 ? kScatterMaxConsumers : 2;
+  const int max_ns = fp8 ? 32 : 4;
   for (int pass = 0; pass < 2 && *NS == 0; ++pass) {
     // first at least half the consumers (the quantiser's compute), then any
     for (int nc = max_nc; nc >= (pass == 0 ? (max_nc + 1) / 2 : 1); --nc) {
       const size_t fixed = scatter_block_bytes(H, scatter_head_ints(mode, R, E), fp8, 0, nc);
       if (fixed >= smem_limit) continue;
       int ns = static_cast<int>((smem_limit - fixed) / (20 + 2 * static_cast<size_t>(H)));
-      if (ns > 32) ns = 32;
+      if (ns > max_ns) ns = max_ns;
       while (ns >= 2 && scatter_block_bytes(H, scatter_head_ints(mode, R, E), fp8, ns, nc) > smem_limit) --ns;
       ns -= ns % nc;  // consumer c owns the stages s = c (mod nc): see the kernel
       if (ns >= 2 && ns >= nc && ns > *NS) {  // the most stages; more consumers on a tie
