@@ -384,7 +384,7 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
       // for small batches -- whose destinations its consumers read from
       // shared memory; then claims of the rest: claim c names position
       // F0 + c % rem of block c / rem (rem = tpb - F0 tokens per block),
-      // kClaimTokens at a time, one claim ahead
+      // a.claim_tokens at a time, one claim ahead
       unsigned* claim = a.barrier + kCtlClaim;
       const int F0 = min(a.own_first, tpb);
       const int rem = tpb - F0;
@@ -403,15 +403,15 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
       };
       for (int tl = 0; ok && tl < min(F0, n_own); ++tl) ok = put(t_begin + tl);
       if (ok && rem > 0) {
-        int base = static_cast<int>(atomicAdd(claim, static_cast<unsigned>(kClaimTokens)));
-        int next = base < cmax ? static_cast<int>(atomicAdd(claim, static_cast<unsigned>(kClaimTokens))) : cmax;
+        int base = static_cast<int>(atomicAdd(claim, static_cast<unsigned>(a.claim_tokens)));
+        int next = base < cmax ? static_cast<int>(atomicAdd(claim, static_cast<unsigned>(a.claim_tokens))) : cmax;
         while (ok && base < cmax) {
-          for (int c = base; ok && c < base + kClaimTokens && c < cmax; ++c) {
+          for (int c = base; ok && c < base + a.claim_tokens && c < cmax; ++c) {
             const int t = (c / rem) * tpb + F0 + c % rem;
             if (t < a.T) ok = put(t);
           }
           base = next;
-          if (base < cmax) next = static_cast<int>(atomicAdd(claim, static_cast<unsigned>(kClaimTokens)));
+          if (base < cmax) next = static_cast<int>(atomicAdd(claim, static_cast<unsigned>(a.claim_tokens)));
         }
       }
       for (int j = i; ok && j < i + NC; ++j) {
@@ -1032,7 +1032,9 @@ cudaError_t configure_fused(size_t optin) {
   return cudaSuccess;
 }
 
-cudaError_t launch_fused(const FusedArgs& a, bool fp8, int mode, int blocks, int NS, int NC, cudaStream_t stream) {
+cudaError_t launch_fused(const FusedArgs& args, bool fp8, int mode, int blocks, int NS, int NC, cudaStream_t stream) {
+  FusedArgs a = args;
+  a.claim_tokens = claim_tokens_for(row_bytes_per_token(a.H, a.k, a.kmax, fp8, mode));
   int kp = 1;
   while (kp < a.k) kp <<= 1;
   const int tpb = fused_tokens_per_block(a.T, blocks);

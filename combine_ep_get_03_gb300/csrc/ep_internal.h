@@ -118,7 +118,19 @@ const void* combine_kernel(int src, bool fp8);
 // last block to finish a launch resets [0], [2], [3] and (fused kernel)
 // advances [1].
 constexpr int kCtlClaim = 2, kCtlDone = 3, kCtlPub = 4;
-constexpr int kClaimTokens = 1;  // tokens per claim (fused V3 dispatch 89.0 -> 86.6 us against 2 per claim; 4 was slower)
+// Tokens per row claim: as few as the claim counter allows.  One atomic on
+// one address completes about every 3.5 ns, so the claims must come at most
+// about every 8 ns over a launch that moves its bytes at ~6 TB/s: a token
+// moving b bytes takes b / 6000 ns of the GPU's time, hence
+// ceil(48000 / b) tokens per claim.  Rows of the V3 shape move 53-90 KB a
+// token: one per claim (fused V3 FP8 dispatch 89.0 -> 86.6 us against two,
+// four slower still); 512-channel rows move ~5 KB: ten per claim (one per
+// claim caps 81 920 tokens at ~330 us, the counter's rate).
+long long row_bytes_per_token(int H, int k, int kmax, bool fp8, int mode);
+inline int claim_tokens_for(long long bytes_per_token) {
+  const long long c = bytes_per_token > 0 ? (48000 + bytes_per_token - 1) / bytes_per_token : 1;
+  return c < 1 ? 1 : (c > 64 ? 64 : static_cast<int>(c));
+}
 // Rows a fused-kernel producer streams in, in the rank-major mode, before its
 // own block's prefixes are final: more would queue ahead of the routing's
 // dependent loads.
@@ -154,6 +166,7 @@ struct ScatterArgs {
   void* recv_x;
   float* recv_scales;
   unsigned* ctl;               // control words (row claims)
+  int claim_tokens;            // tokens per claim (claim_tokens_for)
   int* err;
 };
 // NS row stages and NC consumer warps that fit `smem_limit` (NS = 0: the
@@ -174,6 +187,7 @@ struct FusedArgs {
   int ids32;
   int redundant;               // small batch: every block counts every entry, no grid barrier
   int own_first;               // own tokens a block streams before claiming others' (>= tokens per block: no claims)
+  int claim_tokens;            // tokens per claim (claim_tokens_for)
   const uint16_t* x;
   const float* topk_weights;
   int T, R, E, El, k, kp_log2, kmax, H, M;

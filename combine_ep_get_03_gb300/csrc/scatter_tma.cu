@@ -97,16 +97,16 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_scatter(
   __syncthreads();
 
   if (warp == 0) {
-    // producer: claims tokens kClaimTokens at a time (one claim ahead); when
+    // producer: claims tokens a.claim_tokens at a time (one claim ahead); when
     // the claims run out it hands every consumer warp a "no more" stage
     if (lane == 0) {
       unsigned* claim = a.ctl + kCtlClaim;
-      int base = static_cast<int>(atomicAdd(claim, static_cast<unsigned>(kClaimTokens)));
-      int next = base < a.T ? static_cast<int>(atomicAdd(claim, static_cast<unsigned>(kClaimTokens))) : a.T;
+      int base = static_cast<int>(atomicAdd(claim, static_cast<unsigned>(a.claim_tokens)));
+      int next = base < a.T ? static_cast<int>(atomicAdd(claim, static_cast<unsigned>(a.claim_tokens))) : a.T;
       int i = 0;
       bool ok = true;
       while (ok && base < a.T) {
-        for (int c = 0; c < kClaimTokens && base + c < a.T; ++c, ++i) {
+        for (int c = 0; c < a.claim_tokens && base + c < a.T; ++c, ++i) {
           const int s = i % NS;
           if (i >= NS && !mbar_wait(empty + s, static_cast<uint32_t>((i / NS - 1) & 1), a.err)) {
             ok = false;
@@ -117,7 +117,7 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_scatter(
           bulk_load(stage(s), a.x + static_cast<size_t>(base + c) * H, row_bytes, full + s);
         }
         base = next;
-        if (base < a.T) next = static_cast<int>(atomicAdd(claim, static_cast<unsigned>(kClaimTokens)));
+        if (base < a.T) next = static_cast<int>(atomicAdd(claim, static_cast<unsigned>(a.claim_tokens)));
       }
       for (int j = i; ok && j < i + NC; ++j) {
         const int s = j % NS;
@@ -294,7 +294,16 @@ cudaError_t configure_scatter(size_t optin) {
   return cudaSuccess;
 }
 
-void launch_scatter(const ScatterArgs& a, bool fp8, int mode, int blocks, int NS, int NC, cudaStream_t stream) {
+// Bytes a token moves: its row read, and a row written per destination (at
+// most kmax ranks, or k entries).
+long long row_bytes_per_token(int H, int k, int kmax, bool fp8, int mode) {
+  const long long out_row = fp8 ? static_cast<long long>(H) + 4LL * (H / 128) : 2LL * H;
+  return 2LL * H + static_cast<long long>(mode == kSrcRanks ? kmax : k) * out_row;
+}
+
+void launch_scatter(const ScatterArgs& args, bool fp8, int mode, int blocks, int NS, int NC, cudaStream_t stream) {
+  ScatterArgs a = args;
+  a.claim_tokens = claim_tokens_for(row_bytes_per_token(a.H, a.k, a.kmax, fp8, mode));
   const size_t smem = scatter_block_bytes(a.H, scatter_head_ints(mode, a.R, a.E), fp8, NS, NC);
   const dim3 grid(blocks), block((NC + 1) * 32);
   if (mode == kSrcLowLatency) {
