@@ -31,7 +31,12 @@
 // e4m3 sources pass through a ring of three register buffers instead: the
 // loads of the next two sources are in flight while one is decoded and
 // summed (84.5 -> 82.0 us back to back on the V3 shape, against two-at-a-time
-// batches with an L2 prefetch of the next two).
+// batches with an L2 prefetch of the next two).  Per item, the sources are
+// put in summation order through a 32-slot shared table per warp (one store
+// and one load a lane, not a ballot per source), and a warp steps to its next
+// item's (token, part) with a carry instead of a 64-bit division: 7 % fewer
+// instructions in the issue-bound e4m3 combine (81.9 -> 75.5 us back to
+// back), bf16 combine 120.5 -> 118.2 us.
 #include <climits>
 
 #include "device_common.cuh"
