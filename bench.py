@@ -64,8 +64,8 @@ KERNEL_SOURCES = {"k_combine<normal>": ["combine.cu", "device_common.cuh", "ep_i
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
 # ncu capture of the V3-shaped workload, keyed by the kernel's source digest:
 # a kernel whose sources changed since its capture reports traffic = null.
-MEASURED_TRAFFIC = {"k_combine<normal>": ("0aae301282b5f17e", 694111744),
-                    "k_route_scatter<fp8>": ("180ad1dc0e2c546e", 382859776)}
+MEASURED_TRAFFIC = {"k_combine<normal>": ("7cfdbb7a25288b6d", 693489664),
+                    "k_route_scatter<fp8>": ("5e89feb1817b6791", 382821632)}
 
 
 def kernel_digest(kernel: str) -> str:
