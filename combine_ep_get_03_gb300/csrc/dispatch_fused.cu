@@ -403,15 +403,20 @@ __global__ void __launch_bounds__((kScatterMaxConsumers + 1) * 32, 1) k_route_sc
       };
       for (int tl = 0; ok && tl < min(F0, n_own); ++tl) ok = put(t_begin + tl);
       if (ok && rem > 0) {
-        int base = static_cast<int>(atomicAdd(claim, static_cast<unsigned>(a.claim_tokens)));
-        int next = base < cmax ? static_cast<int>(atomicAdd(claim, static_cast<unsigned>(a.claim_tokens))) : cmax;
-        while (ok && base < cmax) {
-          for (int c = base; ok && c < base + a.claim_tokens && c < cmax; ++c) {
-            const int t = (c / rem) * tpb + F0 + c % rem;
-            if (t < a.T) ok = put(t);
+        // one put() per pass of a single loop (an inner loop over a claim's
+        // tokens compiled to a V3 fused dispatch 3.5 us slower)
+        const int ct = a.claim_tokens;
+        int c = static_cast<int>(atomicAdd(claim, static_cast<unsigned>(ct)));
+        int end = min(c + ct, cmax);
+        int next = c < cmax ? static_cast<int>(atomicAdd(claim, static_cast<unsigned>(ct))) : cmax;
+        while (ok && c < cmax) {
+          const int t = (c / rem) * tpb + F0 + c % rem;
+          if (t < a.T) ok = put(t);
+          if (++c == end) {  // this claim done: take the next, and claim one ahead again
+            c = next;
+            end = min(c + ct, cmax);
+            if (c < cmax) next = static_cast<int>(atomicAdd(claim, static_cast<unsigned>(ct)));
           }
-          base = next;
-          if (base < cmax) next = static_cast<int>(atomicAdd(claim, static_cast<unsigned>(a.claim_tokens)));
         }
       }
       for (int j = i; ok && j < i + NC; ++j) {
