@@ -32,10 +32,11 @@
 // its prefixes are final, so its consumers start on them without waiting for
 // any other block or reading anything back from L2 (a quarter ring beat a
 // full one by 0.8 us on each V3-shaped fused dispatch, one token and half a
-// ring came in between).  Then the producer claims the remaining tokens one
-// at a time from one global counter (claim c names
-// position F0 + c mod (tpb - F0) of block c / (tpb - F0), F0 the tokens each
-// block moves first), one claim ahead, so that an SM that moves rows faster
+// ring came in between).  Then the producer claims the remaining tokens from
+// one global counter, claim_tokens_for(bytes a token moves) at a time (one
+// at the V3 shape) (position c of the claims names position
+// F0 + c mod (tpb - F0) of block c / (tpb - F0), F0 the tokens each block
+// moves first), one claim ahead, so that an SM that moves rows faster
 // takes more of them (the SMs of one GB300 do not all stream at the same
 // rate); a consumer reads a claimed token's destinations from global memory
 // once the owning block has published them.  In the rank-major mode the
