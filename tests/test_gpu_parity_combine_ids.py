@@ -111,6 +111,35 @@ def test_combine_ex_argument_errors():
     h.close()
 
 
+@pytest.mark.parametrize("num_sms", [1, 3])
+def test_combines_with_fewer_warps_than_parts(num_sms):
+    """20 480 channels = 20 work items per token against 16 (bf16, 1 SM), 24
+    (e4m3, 1 SM) or 48 warps: every warp steps its (token, part) by a whole
+    number of tokens plus a remainder of parts, with the carry taken; every
+    combine still equals the oracle."""
+    R, E, k, H, tpr = 4, 16, 4, 20480, 16
+    idx, w, x = _inputs(R, E, k, H, tpr, seed=300 + num_sms)
+    T = idx.shape[0]
+    L = oracle.layout(R, E, k, idx)
+    P = int(L["rank_offset"][-1])
+    y = wl.normal_bf16(wl.rng(301), (P, H))
+    h, _, ref, frac = normal_path(R, E, k, H, idx, w, x, fp8=True, y=y, num_sms=num_sms)
+    assert frac == 1.0
+    rw = (wl.rng(302).random((P, k)) - 0.5).astype(np.float32)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    cw = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    h.combine_ex(dev(ref["recv_x"][:P]), out, y_scales=dev(ref["recv_scales"][:P]), recv_topk_weights=dev(rw),
+                 combined_topk_weights=cw, num_sms=num_sms)
+    ref_out, ref_cw = oracle.combine_ex(R, E, k, idx, ref["recv_x"][:P], y_scales=ref["recv_scales"][:P],
+                                        recv_topk_weights=rw)
+    assert np.array_equal(host_bits(out), ref_out)
+    assert np.array_equal(cw.cpu().numpy().view(np.uint32), ref_cw.view(np.uint32))
+    _, _, lfrac = ll_path(R, E, k, H, idx, w, x, fp8=False, y_seed=303, num_sms=num_sms, handle=h)
+    assert lfrac == 1.0
+    assert h.get_device_status() == ep.EP_OK
+    h.close()
+
+
 # ------------------------------------------------------------ int32 top-k ids
 
 def _handle32(R, E, k, H, tpr):
