@@ -1040,7 +1040,8 @@ cudaError_t configure_fused(size_t optin) {
 
 cudaError_t launch_fused(const FusedArgs& args, bool fp8, int mode, int blocks, int NS, int NC, cudaStream_t stream) {
   FusedArgs a = args;
-  a.claim_tokens = claim_tokens_for(row_bytes_per_token(a.H, a.k, a.kmax, fp8, mode));
+  a.claim_tokens =
+      claim_tokens_for(row_bytes_per_token(a.H, a.k, a.kmax, fp8, mode), mode == kSrcRanks ? blocks : 0);
   int kp = 1;
   while (kp < a.k) kp <<= 1;
   const int tpb = fused_tokens_per_block(a.T, blocks);

@@ -118,17 +118,31 @@ const void* combine_kernel(int src, bool fp8);
 // last block to finish a launch resets [0], [2], [3] and (fused kernel)
 // advances [1].
 constexpr int kCtlClaim = 2, kCtlDone = 3, kCtlPub = 4;
-// Tokens per row claim: as few as the claim counter allows.  One atomic on
-// one address completes about every 3.5 ns, so the claims must come at most
-// about every 8 ns over a launch that moves its bytes at ~6 TB/s: a token
-// moving b bytes takes b / 6000 ns of the GPU's time, hence
-// ceil(48000 / b) tokens per claim.  Rows of the V3 shape move 53-90 KB a
-// token: one per claim (fused V3 FP8 dispatch 89.0 -> 86.6 us against two,
-// four slower still); 512-channel rows move ~5 KB: ten per claim (one per
+// Tokens per row claim: as few as the claim counter and the claim's latency
+// allow.  (1) One atomic on one address completes about every 3.5 ns, so the
+// claims must come at most about every 8 ns over a launch that moves its
+// bytes at ~6 TB/s: a token moving b bytes takes b / 6000 ns of the GPU's
+// time, hence at least ceil(48000 / b) tokens per claim.  (2) With blocks > 0
+// (the rank-major fused kernel, whose tokens are the quickest to move): a
+// producer claims one claim ahead, and a claim's round trip (~1.5 us under
+// load) must not outlast moving the claim's tokens at the block's share of
+// the rate, 6 TB/s / blocks: at least ceil(9e6 / (blocks * b)) tokens.  Rows
+// of the V3 shape move 53-90 KB a token: one per claim on 152 SMs (fused V3
+// FP8 dispatch 89.0 -> 86.6 us against two, four slower still); on 24 SMs
+// the rank-major fused dispatch takes six (312 -> 260 us against one), 64
+// SMs two (130 -> 116 us), while the same rule made the low-latency kernel
+// 1 % slower on 24 SMs and the cached-layout BF16 dispatch 15 % slower on 64
+// (rate-only for them); 512-channel rows move ~5 KB: ten per claim (one per
 // claim caps 81 920 tokens at ~330 us, the counter's rate).
 long long row_bytes_per_token(int H, int k, int kmax, bool fp8, int mode);
-inline int claim_tokens_for(long long bytes_per_token) {
-  const long long c = bytes_per_token > 0 ? (48000 + bytes_per_token - 1) / bytes_per_token : 1;
+inline int claim_tokens_for(long long bytes_per_token, int blocks) {
+  if (bytes_per_token <= 0) return 1;
+  long long c = (48000 + bytes_per_token - 1) / bytes_per_token;
+  if (blocks > 0) {
+    const long long per = static_cast<long long>(blocks) * bytes_per_token;
+    const long long by_latency = (9000000 + per - 1) / per;
+    if (by_latency > c) c = by_latency;
+  }
   return c < 1 ? 1 : (c > 64 ? 64 : static_cast<int>(c));
 }
 // Rows a fused-kernel producer streams in, in the rank-major mode, before its

@@ -303,7 +303,7 @@ long long row_bytes_per_token(int H, int k, int kmax, bool fp8, int mode) {
 
 void launch_scatter(const ScatterArgs& args, bool fp8, int mode, int blocks, int NS, int NC, cudaStream_t stream) {
   ScatterArgs a = args;
-  a.claim_tokens = claim_tokens_for(row_bytes_per_token(a.H, a.k, a.kmax, fp8, mode));
+  a.claim_tokens = claim_tokens_for(row_bytes_per_token(a.H, a.k, a.kmax, fp8, mode), 0);
   const size_t smem = scatter_block_bytes(a.H, scatter_head_ints(mode, a.R, a.E), fp8, NS, NC);
   const dim3 grid(blocks), block((NC + 1) * 32);
   if (mode == kSrcLowLatency) {
