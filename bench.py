@@ -64,8 +64,8 @@ KERNEL_SOURCES = {"k_combine<normal>": ["combine.cu", "device_common.cuh", "ep_i
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
 # ncu capture of the V3-shaped workload, keyed by the kernel's source digest:
 # a kernel whose sources changed since its capture reports traffic = null.
-MEASURED_TRAFFIC = {"k_combine<normal>": ("7cfdbb7a25288b6d", 693489664),
-                    "k_route_scatter<fp8>": ("4ad7005d4445dfb0", 382534656)}
+MEASURED_TRAFFIC = {"k_combine<normal>": ("d3b8e15f1ab358c9", 693772288),
+                    "k_route_scatter<fp8>": ("9ec231528bc7dc3a", 382540544)}
 
 
 def kernel_digest(kernel: str) -> str:
